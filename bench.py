@@ -1,0 +1,461 @@
+"""Benchmark: NVFP4 block-scaled batched GEMV on GB300, through the C ABI.
+
+Default workload: M=7168, K=2048, L=4 (33.1 MB per call), the first of the
+three shapes the submissions time.  One step is one ``nvfp4_gemv`` call,
+the whole hot path.
+
+Timed region (``value``): K back-to-back calls replayed from a CUDA graph,
+bracketed by CUDA events on the launching stream.  Consecutive calls rotate
+over 8 resident copies of the inputs (8 x 33 MB > 2x the 129 MB L2), so every
+call reads its operands from HBM (cold L2).  ``value`` = elapsed / K in
+microseconds per call.
+
+``e2e``: the same call through the C ABI with host buffers: each step copies
+a, b, sfa, sfb from pinned host memory, runs the GEMV and copies c back.
+
+``--impl reference``: the CPU oracle timed on the host cores on a bounded
+sample of the same workload, reported in the same unit.
+
+Run ``python bench.py --all-configs`` to also time every workload and scale
+layout (extra JSON lines, after the main one).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from nvfp4_block_scaled_gemv_gb300 import synthetic  # noqa: E402
+
+METRIC = "us/call (cold L2) and achieved HBM GB/s as % of GB300 peak, NVFP4 GEMV"
+UNIT = "us/call"
+WORKLOAD = synthetic.WORKLOADS[1]  # ("M7168_K2048_L4", 7168, 2048, 4)
+ROTATE_SETS = 8
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=192000)
+    ap.add_argument("--warmup", type=int, default=6400)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--layout", choices=["plain", "permuted"], default="plain")
+    ap.add_argument("--all-configs", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# ranks (replicas only: each rank runs the whole workload on its own GPU)
+# ---------------------------------------------------------------------------
+
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float) -> float:
+    """Largest value of x over all ranks (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    def __init__(self, gpu_id: str, interval_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", gpu_id, "-lms", str(interval_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.monotonic(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        if not inside:
+            inside = [p for _, p in self.samples]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                    "samples": 0}
+        sm = [float(p[1]) for p in inside if p[1].replace(".", "", 1).isdigit()]
+        smax = [float(p[2]) for p in inside if p[2].replace(".", "", 1).isdigit()]
+        reasons = set()
+        for p in inside:
+            for name, val in zip(REASON_NAMES, p[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+def gpu_id_for_smi(torch, dev_index: int) -> str:
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        if u:
+            return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return vis.split(",")[dev_index].strip()
+    return str(dev_index)
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "nvfp4_block_scaled_gemv_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def profiled_traffic(workload: str, layout: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if the kernel
+    sources are unchanged since it was captured."""
+    path = os.path.join(ROOT, "profiles", "gemv_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    entry = d.get(f"{workload}/{layout}")
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class DeviceProblem:
+    """ROTATE_SETS resident copies of one problem's inputs and outputs."""
+
+    def __init__(self, torch, nv, p, M, K, L, layout, dev, sets):
+        self.M, self.K, self.L, self.layout = M, K, L, layout
+        a = torch.from_numpy(p["a"]).to(dev)
+        b = torch.from_numpy(p["b"]).to(dev)
+        sfa = torch.from_numpy(p["sfa"]).to(dev)
+        sfb = torch.from_numpy(p["sfb"]).to(dev)
+        if layout == nv.SF_PERMUTED_128x4:
+            sfa = nv.repack_scales(sfa)
+            sfb = nv.repack_scales(sfb.view(L, 1, K // 16))
+        self.sets = []
+        for i in range(sets):
+            self.sets.append({
+                "a": a.clone(), "b": b.clone(), "sfa": sfa.clone(), "sfb": sfb.clone(),
+                "c": torch.empty((L, M), dtype=torch.float16, device=dev)})
+        del a, b, sfa, sfb
+
+    def call(self, nv, i, stream_handle):
+        s = self.sets[i % len(self.sets)]
+        nv.nvfp4_gemv(s["a"].data_ptr(), s["b"].data_ptr(), s["sfa"].data_ptr(),
+                      s["sfb"].data_ptr(), s["c"].data_ptr(), self.M, self.K, self.L,
+                      self.layout, stream_handle)
+
+
+def time_graph(torch, nv, prob, steps, warmup, stream):
+    """Per-call microseconds over `steps` calls replayed from a CUDA graph."""
+    handle = stream.cuda_stream
+    g_size = max(d for d in range(1, min(64, steps) + 1) if steps % d == 0)
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 3)):
+            prob.call(nv, i, handle)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(g_size):
+            prob.call(nv, i, handle)
+    for _ in range(2):
+        graph.replay()
+    stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps // g_size):
+            graph.replay()
+        e1.record(stream)
+    stream.synchronize()
+    t1 = time.monotonic()
+    torch.cuda.synchronize()
+    barrier()
+    return e0.elapsed_time(e1) * 1e3 / steps, (t0, t1), steps
+
+
+def time_single_flushed(torch, nv, prob, reps, stream):
+    """Median microseconds of one event-bracketed call after an L2 flush."""
+    flush = torch.empty(2 * 160 * 2 ** 20, dtype=torch.uint8, device=prob.sets[0]["a"].device)
+    handle = stream.cuda_stream
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(reps):
+            flush.fill_(i & 0xFF)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            prob.call(nv, i, handle)
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3)
+    del flush
+    return statistics.median(times), min(times)
+
+
+def time_e2e(torch, nv, p, M, K, L, dev, steps, stream):
+    """End-to-end per-step microseconds with host buffers (pinned)."""
+    host = {k: torch.from_numpy(v).pin_memory() for k, v in p.items()}
+    d = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    c = torch.empty((L, M), dtype=torch.float16, device=dev)
+    c_host = torch.empty((L, M), dtype=torch.float16).pin_memory()
+    handle = stream.cuda_stream
+
+    def step():
+        for k in ("a", "b", "sfa", "sfb"):
+            d[k].copy_(host[k], non_blocking=True)
+        nv.nvfp4_gemv(d["a"].data_ptr(), d["b"].data_ptr(), d["sfa"].data_ptr(),
+                      d["sfb"].data_ptr(), c.data_ptr(), M, K, L, nv.SF_PLAIN, handle)
+        c_host.copy_(c, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            step()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    stream.synchronize()
+    h2d = sum(v.numel() * v.element_size() for k, v in host.items())
+    d2h = c_host.numel() * c_host.element_size()
+    return e0.elapsed_time(e1) * 1e3 / steps, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline
+# ---------------------------------------------------------------------------
+
+def oracle_us_per_call(p, M, K, L, budget_s: float):
+    """The oracle on one host core over a bounded sample of rows, scaled to a
+    full call.  Returns (us_per_call, sample description)."""
+    import oracle
+
+    rows = L * M
+    n = 256
+    rng = np.random.default_rng(0)
+    spent, done = 0.0, 0
+    while True:
+        li = rng.integers(0, L, n)
+        mi = rng.integers(0, M, n)
+        t0 = time.perf_counter()
+        oracle.gemv_at(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L, mi, li)
+        spent += time.perf_counter() - t0
+        done += n
+        if spent >= budget_s:
+            break
+        n = min(8192, n * 2)
+    us = spent / done * rows * 1e6
+    return us, (f"{done} random outputs (full K each) of the {rows}-output call in {spent:.2f} s "
+                "on one core, scaled to the whole call")
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return
+    name, M, K, L = WORKLOAD
+    p = synthetic.make_problem(M, K, L, seed=0)
+    # every step is one bounded sample; the whole run stays within about a minute
+    per_step_budget = max(0.02, min(10.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_us_per_call(p, M, K, L, per_step_budget / 4)
+    vals, samples = [], []
+    for _ in range(args.steps):
+        us, sample = oracle_us_per_call(p, M, K, L, per_step_budget)
+        vals.append(us)
+        samples.append(sample)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(value / 1e3, 6), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "M": M, "K": K, "L": L, "scale_layout": "plain"},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": samples[-1]},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_native(args):
+    import torch
+
+    import nvfp4_block_scaled_gemv_gb300 as nv
+    from nvfp4_block_scaled_gemv_gb300 import build as libbuild
+
+    rank, world, local = rank_info()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    libbuild.build()
+    nv.library()
+    stream = torch.cuda.Stream(device=dev)
+
+    name, M, K, L = WORKLOAD
+    layout = nv.SF_PLAIN if args.layout == "plain" else nv.SF_PERMUTED_128x4
+    p = synthetic.make_problem(M, K, L, seed=0)
+    prob = DeviceProblem(torch, nv, p, M, K, L, layout, dev, ROTATE_SETS)
+    nbytes = synthetic.algorithmic_bytes(M, K, L)
+
+    sampler = ClockSampler(gpu_id_for_smi(torch, local)) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    us, (t0, t1), steps = time_graph(torch, nv, prob, args.steps, args.warmup, stream)
+    if sampler:
+        sampler.stop()
+    us_job = max_over_ranks(us * steps) / (steps * world)  # all ranks' calls / slowest rank
+    us_rank = max_over_ranks(us)
+
+    single_med, single_min = time_single_flushed(torch, nv, prob, 50, stream)
+    e2e_us, h2d, d2h = time_e2e(torch, nv, p, M, K, L, dev, args.e2e_steps, stream)
+    e2e_us = max_over_ranks(e2e_us)
+
+    if rank != 0:
+        return
+    cpu_us, cpu_sample = oracle_us_per_call(p, M, K, L, budget_s=10.0)
+    peaks = measured_peaks()
+    achieved = nbytes / (us_rank * 1e-6) / 1e9
+    plan = nv.nvfp4_gemv_plan(M, K, L, layout, torch.cuda.get_device_properties(dev).multi_processor_count)
+    line = {
+        "metric": METRIC, "value": round(us_job, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us_job / 1e3, 7),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e2m1xe4m3->f32->f16", "data": "synthetic",
+        "config": {"workload": name, "M": M, "K": K, "L": L, "scale_layout": args.layout,
+                   "l2": f"{ROTATE_SETS} rotating input sets, {ROTATE_SETS * nbytes / 1e6:.0f} MB "
+                         "> 2x L2 (cold L2 every call)",
+                   "launch": "CUDA graph of back-to-back nvfp4_gemv calls, PDL",
+                   "bytes_per_call": nbytes, "schedule": plan},
+        "gb_per_s": round(achieved, 1),
+        "pct_of_hbm_peak": round(100 * achieved / peaks["hbm_gbs"], 2),
+        "single_call_l2_flushed_us": {"median": round(single_med, 3), "min": round(single_min, 3)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": profiled_traffic(name, args.layout),
+                     "peak_source": peaks["source"]},
+        "cpu_baseline": {"value": round(cpu_us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": cpu_sample},
+        "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": steps,
+        "clocks": sampler.summary(t0, t1) if sampler else None,
+    }
+    print(json.dumps(line), flush=True)
+
+    if args.all_configs:
+        for wname, wM, wK, wL in synthetic.WORKLOADS:
+            wp = synthetic.make_problem(wM, wK, wL, seed=0)
+            wbytes = synthetic.algorithmic_bytes(wM, wK, wL)
+            sets = max(2, min(ROTATE_SETS, -(-400 * 2 ** 20 // wbytes)))
+            for lay_name, lay in (("plain", nv.SF_PLAIN), ("permuted", nv.SF_PERMUTED_128x4)):
+                wprob = DeviceProblem(torch, nv, wp, wM, wK, wL, lay, dev, sets)
+                wsteps = max(64, min(20000, int(2e9 / wbytes)) // 64 * 64)
+                wus, _, _ = time_graph(torch, nv, wprob, wsteps, 64, stream)
+                smed, smin = time_single_flushed(torch, nv, wprob, 20, stream)
+                gbs = wbytes / (wus * 1e-6) / 1e9
+                print(json.dumps({"workload": wname, "scale_layout": lay_name,
+                                  "us_per_call": round(wus, 3), "gb_per_s": round(gbs, 1),
+                                  "pct_of_hbm_peak": round(100 * gbs / peaks["hbm_gbs"], 2),
+                                  "rotating_sets": sets, "calls": wsteps,
+                                  "single_call_l2_flushed_us": round(smed, 3)}), flush=True)
+                del wprob
+                torch.cuda.empty_cache()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

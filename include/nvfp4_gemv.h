@@ -1,0 +1,153 @@
+/*
+ * nvfp4_gemv.h: C ABI of the GB300 (sm_103a) NVFP4 block-scaled batched GEMV.
+ *
+ * The operation (kernelbot "nvfp4-gemv" submission 103289, `cute_kernel`:
+ * each output accumulates a*sfa*b*sfb over K in FP32 and is stored with
+ * `.to(Float16)`; submission 69953's docstring names the shapes):
+ *
+ *   c[m,l] = fp16( sum_{k<K} E2M1(a[m,k,l]) * E4M3(sfa[m,k/16,l])
+ *                          * E2M1(b[k,l])   * E4M3(sfb[k/16,l]) )
+ *
+ * Element formats: E2M1 is FP4 (sign, 2 exponent bits, 1 mantissa bit; no
+ * Inf/NaN); E4M3 is finite-only FP8 (0x7F/0xFF are NaN).  Two E2M1 codes are
+ * packed per byte along K, the lower k in the low nibble (the pages' torch
+ * tensors are `float4_e2m1fn_x2`, so "k is halved").  One E4M3 scale covers
+ * 16 consecutive K elements (`sf_vec_size = 16`).
+ *
+ * Memory layouts (all row-major, batch L outermost; submission 103289's
+ * `cute_jit_kernel` gives A the strides (k, 1, m*k) and c the strides
+ * (1, 1, m)):
+ *   a   : uint8 [L][M][K/2]          packed E2M1, row stride K/2 bytes
+ *   b   : uint8 [L][K/2]             packed E2M1 (dense: no N padding)
+ *   c   : fp16  [L][M]               output, written, never read
+ *   sfa, sfb in one of two layouts, chosen by `sf_layout`:
+ *     NVFP4_SF_PLAIN          sfa uint8 [L][M][K/16], sfb uint8 [L][K/16]
+ *     NVFP4_SF_PERMUTED_128x4 the pre-permuted tensor [32, 4, rest_m, 4,
+ *        rest_k, L] of submission 103289 (`permuted_to_blocked`), stored
+ *        L-outermost in 128x4 atoms of 512 bytes: byte (m, kb) of batch l is
+ *        at ((l*rest_m + m/128)*rest_k + kb/4)*512 + (m%32)*16
+ *        + ((m/32)%4)*4 + kb%4, rest_m = ceil(rows/128), rest_k = K/64.
+ *        For sfb, rows = 1 (row 0 of each atom is used).
+ *        nvfp4_repack_scales() produces this layout from the plain one.
+ *
+ * Ownership and execution: every pointer is device memory owned by the
+ * caller (or memory the device can address, such as mapped pinned host
+ * memory).  No call allocates, frees, synchronizes or keeps per-call state;
+ * all work is enqueued on `stream` (NULL = the legacy default stream), so
+ * calls may be captured into CUDA graphs.  Kernels are launched with
+ * programmatic stream serialization: they wait for the preceding work on the
+ * stream before reading any input, so stream order is preserved.
+ *
+ * Errors: arguments are validated on the host before anything is launched,
+ * and a failing call launches nothing unless it returns NVFP4_ERR_CUDA.
+ */
+#ifndef NVFP4_GEMV_H
+#define NVFP4_GEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t is a pointer to this opaque driver type. */
+struct CUstream_st;
+
+typedef enum {
+  NVFP4_SF_PLAIN = 0,
+  NVFP4_SF_PERMUTED_128x4 = 1
+} nvfp4_sf_layout_t;
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_VALUE = 1,     /* NULL pointer with non-empty data, negative size, bad enum */
+  NVFP4_ERR_UNSUPPORTED_SHAPE = 2, /* K % 64 != 0, or a size beyond the limits below */
+  NVFP4_ERR_MISALIGNED = 3,        /* pointer alignment rule broken (see each call) */
+  NVFP4_ERR_CUDA = 4               /* a CUDA runtime call failed; see nvfp4_last_cuda_error() */
+} nvfp4_status_t;
+
+/*
+ * Batched GEMV, c[m,l] as defined above.
+ *
+ *   a, b, sfa, sfb : inputs in the layouts above (sf_layout selects the scale layout)
+ *   c              : output, fp16 [L][M]
+ *   M, K, L        : rows, reduction length (elements), batch count
+ *   sf_layout      : NVFP4_SF_PLAIN or NVFP4_SF_PERMUTED_128x4
+ *   stream         : CUDA stream (cudaStream_t)
+ *
+ * Shapes: M, L >= 0 and K >= 0 with K % 64 == 0 (the pages' K tile and
+ * scale atom, `mma_tiler_mnk = (128, 1, 64)`).  M == 0 or L == 0 is a no-op
+ * (pointers may be NULL).  K == 0 writes +0 to every c (a, b, sfa, sfb may be
+ * NULL).  Limits: K <= 2^30, M*L < 2^40.
+ * Alignment: a, b, sfa, sfb 32-byte aligned; c 2-byte aligned.
+ * Accuracy: each 16-element block's dot product is exact; blocks are scaled
+ * and summed in FP32; c is rounded to nearest even (overflow gives +-Inf;
+ * a NaN scale gives NaN).  Results are bitwise reproducible run to run, and
+ * identical for the two scale layouts.
+ */
+nvfp4_status_t nvfp4_gemv(const void* a, const void* b, const void* sfa, const void* sfb,
+                          void* c, int64_t M, int64_t K, int64_t L, int sf_layout,
+                          struct CUstream_st* stream);
+
+/*
+ * nvfp4_gemv with the launch schedule given instead of chosen (for tuning
+ * and for testing every schedule; same arguments, rules and results
+ * contract as nvfp4_gemv).  lanes_per_row in {4, 8, 16, 32}: lanes sharing a
+ * row; k_split in {1, 2, 4, 8}: warps splitting a row's K range; ctas in
+ * [1, 2^31): grid size.  The summation order, and so the last bits of c,
+ * depend on (lanes_per_row, k_split); any valid schedule meets the accuracy
+ * contract.  Invalid schedule values give NVFP4_ERR_INVALID_VALUE.
+ */
+nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa,
+                                   const void* sfb, void* c, int64_t M, int64_t K, int64_t L,
+                                   int sf_layout, int lanes_per_row, int k_split, int64_t ctas,
+                                   struct CUstream_st* stream);
+
+/*
+ * Scale repack: plain [L][rows][K/16] E4M3 -> the 128x4-atom pre-permuted
+ * layout above (submission 69953, `to_blocked_batch`; submission 69575,
+ * `blocked_transform_kernel`).  A byte permutation, bit-exact; padding rows
+ * rows..128*rest_m-1 of the last atom row are written as 0x00.  dst must hold
+ * nvfp4_permuted_scale_bytes(rows, K, L) bytes and must not overlap src.
+ * Use rows = M for sfa and rows = 1 for sfb.
+ * Shapes: rows, L >= 0, K % 64 == 0 (empty is a no-op).
+ * Alignment: src 4-byte aligned; dst 16-byte aligned.
+ */
+nvfp4_status_t nvfp4_repack_scales(const void* src, void* dst, int64_t rows, int64_t K,
+                                   int64_t L, struct CUstream_st* stream);
+
+/* Bytes of a permuted scale tensor: L * ceil(rows/128) * (K/64) * 512.
+ * Returns 0 for invalid arguments (negative sizes or K % 64 != 0). */
+size_t nvfp4_permuted_scale_bytes(int64_t rows, int64_t K, int64_t L);
+
+/* Static, human-readable name of a status code. */
+const char* nvfp4_status_string(int status);
+
+/* The cudaError_t of the most recent NVFP4_ERR_CUDA on the calling thread
+ * (0 if none). */
+int nvfp4_last_cuda_error(void);
+
+/*
+ * Launch plan of nvfp4_gemv, computed on the host only (no GPU needed), for
+ * inspection and tests.  num_sms is the device's multiprocessor count and
+ * ctas_per_sm the number of the kernel's CTAs resident per SM (pass 0 to use
+ * the compiled-in default).
+ */
+typedef struct {
+  int lanes_per_row;  /* lanes of a warp that share one row (32-byte K chunk each) */
+  int k_split;        /* warps of a CTA that split one row's K range */
+  int rows_per_pass;  /* rows a warp reduces at once (<= 8) */
+  int threads_per_cta;
+  int64_t ctas;       /* grid size */
+  int64_t steps;      /* K chunks per lane per row, ceil(K/64 / lanes_per_row) */
+} nvfp4_gemv_plan_t;
+
+nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, int num_sms,
+                               int ctas_per_sm, nvfp4_gemv_plan_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GEMV_H */

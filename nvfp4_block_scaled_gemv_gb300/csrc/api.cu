@@ -1,0 +1,245 @@
+// C ABI: argument validation, launch planning and dispatch.
+#include <atomic>
+#include <cstdint>
+
+#include "internal.h"
+#include "nvfp4_gemv.h"
+
+namespace nvfp4 {
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+constexpr int kMaxDevices = 128;
+std::atomic<int> g_sms[kMaxDevices];
+std::atomic<int> g_gemv_occ[kMaxDevices];
+std::atomic<int> g_repack_occ[kMaxDevices];
+
+constexpr int64_t kMaxK = int64_t(1) << 30;
+constexpr int64_t kMaxRows = int64_t(1) << 40;  // M * L
+constexpr int64_t kMaxM = (int64_t(1) << 31) - 1;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+nvfp4_status_t cuda_failure(cudaError_t err) {
+  g_last_cuda_error = (int)err;
+  (void)cudaGetLastError();  // clear a non-sticky launch error
+  return NVFP4_ERR_CUDA;
+}
+
+// Multiprocessor count and kernel occupancies of the current device, cached
+// per device (a benign race: concurrent first calls store the same values).
+cudaError_t device_info(int* sms, int* gemv_occ, int* repack_occ) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  int s = g_sms[dev].load(std::memory_order_relaxed);
+  int g = g_gemv_occ[dev].load(std::memory_order_relaxed);
+  int r = g_repack_occ[dev].load(std::memory_order_relaxed);
+  if (s <= 0 || g <= 0 || r <= 0) {
+    err = cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    err = gemv_ctas_per_sm(&g);
+    if (err != cudaSuccess) return err;
+    err = repack_ctas_per_sm(&r);
+    if (err != cudaSuccess) return err;
+    if (g < 1) g = 1;
+    if (r < 1) r = 1;
+    g_sms[dev].store(s, std::memory_order_relaxed);
+    g_gemv_occ[dev].store(g, std::memory_order_relaxed);
+    g_repack_occ[dev].store(r, std::memory_order_relaxed);
+  }
+  if (sms) *sms = s;
+  if (gemv_occ) *gemv_occ = g;
+  if (repack_occ) *repack_occ = r;
+  return cudaSuccess;
+}
+
+nvfp4_status_t validate_gemv_shape(int64_t M, int64_t K, int64_t L, int sf_layout) {
+  if (M < 0 || K < 0 || L < 0) return NVFP4_ERR_INVALID_VALUE;
+  if (sf_layout != NVFP4_SF_PLAIN && sf_layout != NVFP4_SF_PERMUTED_128x4)
+    return NVFP4_ERR_INVALID_VALUE;
+  if (K % 64 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (K > kMaxK || M > kMaxM) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (M != 0 && L > kMaxRows / M) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return NVFP4_OK;
+}
+
+nvfp4_status_t validate_gemv_pointers(const void* a, const void* b, const void* sfa,
+                                      const void* sfb, const void* c, int64_t K) {
+  if (c == nullptr) return NVFP4_ERR_INVALID_VALUE;
+  if (K > 0 && (a == nullptr || b == nullptr || sfa == nullptr || sfb == nullptr))
+    return NVFP4_ERR_INVALID_VALUE;
+  if (!aligned(c, 2)) return NVFP4_ERR_MISALIGNED;
+  if (K > 0 && (!aligned(a, 32) || !aligned(b, 32) || !aligned(sfa, 32) || !aligned(sfb, 32)))
+    return NVFP4_ERR_MISALIGNED;
+  return NVFP4_OK;
+}
+
+GemvParams make_params(const void* a, const void* b, const void* sfa, const void* sfb, void* c,
+                       int64_t M, int64_t K, int64_t L, bool permuted, const GemvPlan& plan) {
+  GemvParams p;
+  p.a = static_cast<const uint8_t*>(a);
+  p.b = static_cast<const uint8_t*>(b);
+  p.sfa = static_cast<const uint8_t*>(sfa);
+  p.sfb = static_cast<const uint8_t*>(sfb);
+  p.c = static_cast<uint16_t*>(c);
+  p.M = M;
+  p.rest_m = (int32_t)((M + 127) / 128);
+  p.rest_k = (int32_t)(K / 64);
+  p.rows_per_l = permuted ? (int64_t)p.rest_m * 128 : M;
+  p.rows_total = p.rows_per_l * L;
+  p.half_k = (int32_t)(K / 2);
+  p.blocks = (int32_t)(K / 16);
+  p.kchunks = (int32_t)(K / 64);
+  p.steps = (int32_t)plan.steps;
+  return p;
+}
+
+nvfp4_status_t run_gemv(const void* a, const void* b, const void* sfa, const void* sfb, void* c,
+                        int64_t M, int64_t K, int64_t L, int sf_layout, const GemvPlan& plan,
+                        cudaStream_t stream) {
+  const bool permuted = sf_layout == NVFP4_SF_PERMUTED_128x4;
+  const GemvParams p = make_params(a, b, sfa, sfb, c, M, K, L, permuted, plan);
+  cudaError_t err = permuted ? launch_gemv_permuted(p, plan, stream)
+                             : launch_gemv_plain(p, plan, stream);
+  if (err != cudaSuccess) return cuda_failure(err);
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+// The schedule (see gemv_kernel.cuh for what each knob means):
+//  * lanes_per_row: the width among 32/16/8/4 lanes that leaves the fewest
+//    idle lane slots over K/64 chunks (ties go to the wider one);
+//  * ctas: one wave of resident CTAs (SMs x occupancy), fewer for tiny
+//    problems (at least 8 rows per CTA);
+//  * k_split: the smallest split that still gives each row lane of 8/k_split
+//    warps a full pass of 8 rows, capped by the number of chunk steps.
+bool plan_gemv(int64_t M, int64_t K, int64_t L, int num_sms, int ctas_per_sm, GemvPlan* out) {
+  if (M < 0 || K < 0 || L < 0 || num_sms < 1 || ctas_per_sm < 1 || out == nullptr) return false;
+  const int64_t kchunks = K / 64;
+  int lpr = 32;
+  int64_t best_slots = -1;
+  for (int cand : {32, 16, 8, 4}) {
+    const int64_t slots = (kchunks + cand - 1) / cand * cand;
+    if (best_slots < 0 || slots < best_slots) {
+      best_slots = slots;
+      lpr = cand;
+    }
+  }
+  const int64_t steps = (kchunks + lpr - 1) / lpr;
+  const int64_t rows = M * L;
+  int64_t ctas = (int64_t)num_sms * ctas_per_sm;
+  const int64_t by_rows = (rows + kRowsPerPass - 1) / kRowsPerPass;
+  if (by_rows < ctas) ctas = by_rows;
+  if (ctas < 1) ctas = 1;
+  int ks = 1;
+  while (ks < kGemvWarps && 2 * ks <= steps && rows * ks < ctas * kGemvWarps * kRowsPerPass)
+    ks *= 2;
+  out->lanes_per_row = lpr;
+  out->k_split = ks;
+  out->ctas = ctas;
+  out->steps = steps;
+  return true;
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" {
+
+nvfp4_status_t nvfp4_gemv(const void* a, const void* b, const void* sfa, const void* sfb,
+                          void* c, int64_t M, int64_t K, int64_t L, int sf_layout,
+                          struct CUstream_st* stream) {
+  nvfp4_status_t st = validate_gemv_shape(M, K, L, sf_layout);
+  if (st != NVFP4_OK) return st;
+  if (M == 0 || L == 0) return NVFP4_OK;
+  st = validate_gemv_pointers(a, b, sfa, sfb, c, K);
+  if (st != NVFP4_OK) return st;
+  int sms = 0, occ = 0;
+  cudaError_t err = device_info(&sms, &occ, nullptr);
+  if (err != cudaSuccess) return cuda_failure(err);
+  GemvPlan plan;
+  if (!plan_gemv(M, K, L, sms, occ, &plan)) return NVFP4_ERR_INVALID_VALUE;
+  return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, (cudaStream_t)stream);
+}
+
+nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa,
+                                   const void* sfb, void* c, int64_t M, int64_t K, int64_t L,
+                                   int sf_layout, int lanes_per_row, int k_split, int64_t ctas,
+                                   struct CUstream_st* stream) {
+  nvfp4_status_t st = validate_gemv_shape(M, K, L, sf_layout);
+  if (st != NVFP4_OK) return st;
+  if (lanes_per_row != 4 && lanes_per_row != 8 && lanes_per_row != 16 && lanes_per_row != 32)
+    return NVFP4_ERR_INVALID_VALUE;
+  if (k_split != 1 && k_split != 2 && k_split != 4 && k_split != 8) return NVFP4_ERR_INVALID_VALUE;
+  if (ctas < 1 || ctas > 0x7fffffff) return NVFP4_ERR_INVALID_VALUE;
+  if (M == 0 || L == 0) return NVFP4_OK;
+  st = validate_gemv_pointers(a, b, sfa, sfb, c, K);
+  if (st != NVFP4_OK) return st;
+  GemvPlan plan;
+  plan.lanes_per_row = lanes_per_row;
+  plan.k_split = k_split;
+  plan.ctas = ctas;
+  plan.steps = (K / 64 + lanes_per_row - 1) / lanes_per_row;
+  return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, (cudaStream_t)stream);
+}
+
+nvfp4_status_t nvfp4_repack_scales(const void* src, void* dst, int64_t rows, int64_t K,
+                                   int64_t L, struct CUstream_st* stream) {
+  if (rows < 0 || K < 0 || L < 0) return NVFP4_ERR_INVALID_VALUE;
+  if (K % 64 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (K > kMaxK || rows > kMaxM) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (rows != 0 && L > kMaxRows / rows) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0 || K == 0 || L == 0) return NVFP4_OK;
+  if (src == nullptr || dst == nullptr) return NVFP4_ERR_INVALID_VALUE;
+  if (!aligned(src, 4) || !aligned(dst, 16)) return NVFP4_ERR_MISALIGNED;
+  int sms = 0, occ = 0;
+  cudaError_t err = device_info(&sms, nullptr, &occ);
+  if (err != cudaSuccess) return cuda_failure(err);
+  err = launch_repack(static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), rows, K, L,
+                      (int64_t)sms * occ, (cudaStream_t)stream);
+  if (err != cudaSuccess) return cuda_failure(err);
+  return NVFP4_OK;
+}
+
+size_t nvfp4_permuted_scale_bytes(int64_t rows, int64_t K, int64_t L) {
+  if (rows < 0 || K < 0 || L < 0 || K % 64 != 0) return 0;
+  return (size_t)(L * ((rows + 127) / 128) * (K / 64) * 512);
+}
+
+const char* nvfp4_status_string(int status) {
+  switch (status) {
+    case NVFP4_OK: return "NVFP4_OK";
+    case NVFP4_ERR_INVALID_VALUE: return "NVFP4_ERR_INVALID_VALUE";
+    case NVFP4_ERR_UNSUPPORTED_SHAPE: return "NVFP4_ERR_UNSUPPORTED_SHAPE";
+    case NVFP4_ERR_MISALIGNED: return "NVFP4_ERR_MISALIGNED";
+    case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA";
+    default: return "NVFP4_ERR_UNKNOWN";
+  }
+}
+
+int nvfp4_last_cuda_error(void) { return g_last_cuda_error; }
+
+nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, int num_sms,
+                               int ctas_per_sm, nvfp4_gemv_plan_t* out) {
+  if (out == nullptr || num_sms < 1 || ctas_per_sm < 0) return NVFP4_ERR_INVALID_VALUE;
+  nvfp4_status_t st = validate_gemv_shape(M, K, L, sf_layout);
+  if (st != NVFP4_OK) return st;
+  GemvPlan plan;
+  if (!plan_gemv(M, K, L, num_sms, ctas_per_sm > 0 ? ctas_per_sm : kGemvMinCtasPerSm, &plan))
+    return NVFP4_ERR_INVALID_VALUE;
+  out->lanes_per_row = plan.lanes_per_row;
+  out->k_split = plan.k_split;
+  out->rows_per_pass = kRowsPerPass;
+  out->threads_per_cta = kGemvThreads;
+  out->ctas = plan.ctas;
+  out->steps = plan.steps;
+  return NVFP4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,15 @@
+// GEMV kernels for plain [L][M][K/16] scales, plus the occupancy query.
+#include "gemv_kernel.cuh"
+
+namespace nvfp4 {
+
+cudaError_t launch_gemv_plain(const GemvParams& p, const GemvPlan& plan, cudaStream_t stream) {
+  return launch_gemv_layout<false>(p, plan, stream);
+}
+
+cudaError_t gemv_ctas_per_sm(int* out) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, nvfp4_gemv_kernel<32, 1, false>,
+                                                       kGemvThreads, 0);
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,55 @@
+// Host/device interface between the C ABI layer and the kernels.
+#pragma once
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+constexpr int kGemvThreads = 256;   // 8 warps per CTA
+constexpr int kGemvWarps = kGemvThreads / 32;
+constexpr int kGemvMinCtasPerSm = 2;  // __launch_bounds__ occupancy floor
+constexpr int kRowsPerPass = 8;     // rows one warp reduces at once
+
+// Everything a GEMV kernel needs, by value (kernel parameter space).
+struct GemvParams {
+  const uint8_t* a;
+  const uint8_t* b;
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  uint16_t* c;        // fp16 bits
+  int64_t M;
+  int64_t rows_per_l; // rows visited per batch: M (plain) or 128*rest_m (permuted)
+  int64_t rows_total; // rows_per_l * L
+  int32_t half_k;     // K/2: bytes of one packed row
+  int32_t blocks;     // K/16: scale bytes of one plain row
+  int32_t kchunks;    // K/64: 32-byte chunks per row (one per 128x4 atom column)
+  int32_t steps;      // ceil(kchunks / lanes_per_row)
+  int32_t rest_m;     // ceil(M/128)
+  int32_t rest_k;     // K/64
+};
+
+struct GemvPlan {
+  int lanes_per_row;  // 4, 8, 16 or 32
+  int k_split;        // 1, 2, 4 or 8 warps per row range
+  int64_t ctas;
+  int64_t steps;
+};
+
+// Host-only schedule choice (no CUDA calls).  Returns false for shapes the
+// planner cannot handle (caller validates first).
+bool plan_gemv(int64_t M, int64_t K, int64_t L, int num_sms, int ctas_per_sm, GemvPlan* out);
+
+// Occupancy of the GEMV kernel family on the current device (CTAs per SM).
+cudaError_t gemv_ctas_per_sm(int* out);
+
+// Scale repack: occupancy (CTAs per SM) and launch over at most max_ctas CTAs.
+cudaError_t repack_ctas_per_sm(int* out);
+cudaError_t launch_repack(const uint8_t* src, uint8_t* dst, int64_t rows, int64_t K, int64_t L,
+                          int64_t max_ctas, cudaStream_t stream);
+
+// Per-layout GEMV launchers (gemv_plain.cu, gemv_permuted.cu).
+cudaError_t launch_gemv_plain(const GemvParams& p, const GemvPlan& plan, cudaStream_t stream);
+cudaError_t launch_gemv_permuted(const GemvParams& p, const GemvPlan& plan, cudaStream_t stream);
+
+}  // namespace nvfp4

@@ -1,0 +1,88 @@
+// Inline-PTX helpers for sm_103a: streaming loads, packed FP4/FP8 decode,
+// half2 FMA and programmatic-dependent-launch control.
+#pragma once
+#include <cstdint>
+
+namespace nvfp4 {
+
+// 256-bit load of streamed data (read once): bypass L1, ask L2 for 256-byte
+// prefetch granules.  p must be 32-byte aligned.
+__device__ __forceinline__ void ld_stream_256(const void* p, uint32_t (&r)[8]) {
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.L2::256B.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "l"(p));
+}
+
+// 256-bit load of data many warps re-read (the vector b): normal L1 caching.
+__device__ __forceinline__ void ld_shared_256(const void* p, uint32_t (&r)[8]) {
+  asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "l"(p));
+}
+
+// 32-bit load of scale bytes (their 32-byte sectors are shared by
+// neighbouring rows, so L1 allocation is kept).  p must be 4-byte aligned.
+__device__ __forceinline__ uint32_t ld_scale_32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// Two E2M1 codes (low byte of v: low nibble first) -> f16x2 (low half first).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t v) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(out)
+      : "r"(v));
+  return out;
+}
+
+// Two E4M3 codes (low 16 bits of v) -> f16x2.  Exact; NaN stays NaN.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+  uint32_t out;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+      : "=r"(out)
+      : "r"(v));
+  return out;
+}
+
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ float f16_lo_to_f32(uint32_t h) {
+  float f;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}"
+      : "=f"(f)
+      : "r"(h));
+  return f;
+}
+
+__device__ __forceinline__ float f16_hi_to_f32(uint32_t h) {
+  float f;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, hi;\n\t}"
+      : "=f"(f)
+      : "r"(h));
+  return f;
+}
+
+// Programmatic dependent launch: block until the preceding grid on the
+// stream has completed and its writes are visible (a no-op when the launch
+// carries no programmatic dependency).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid on the stream to begin launching.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,89 @@
+// Scale repack: plain [L][rows][K/16] E4M3 bytes -> 128x4-atom layout.
+//
+// The destination is the pre-permuted scale tensor [32, 4, rest_m, 4, rest_k,
+// L] of kernelbot nvfp4-gemv submission 103289 (`permuted_to_blocked`),
+// stored L-outermost so that permuting it to [rest_m, rest_k, 32, 4, 4] is the
+// blocked order that submission 69953's `to_blocked_batch` builds: byte
+// (m, kb) of batch l goes to
+//   ((l*rest_m + m/128)*rest_k + kb/4)*512 + (m%32)*16 + ((m/32)%4)*4 + kb%4.
+// Rows past `rows` in the last 128-row block are written as 0x00.
+//
+// Each tile is one 128-row block by kTileCols atom columns (4 scale bytes per
+// row each).  The tile's source words are read row by row (coalesced, 4-byte
+// loads since plain rows are only 4-byte aligned), staged in shared memory,
+// and written back as whole 512-byte atoms with 16-byte stores.  The grid is
+// sized to the SMs and strides over tiles.
+#include <cstdint>
+
+#include "internal.h"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kRepackThreads = 256;
+constexpr int kTileCols = 16;               // atom columns per tile (64 scale bytes per row)
+constexpr int kTileWords = 128 * kTileCols; // 4-byte words per tile
+constexpr int kPitch = kTileCols + 1;       // odd pitch: conflict-free column gathers
+
+__global__ void __launch_bounds__(kRepackThreads)
+    repack_scales_kernel(const uint32_t* __restrict__ src, uint4* __restrict__ dst, int64_t rows,
+                         int32_t rest_m, int32_t rest_k, int64_t tiles) {
+  __shared__ uint32_t tile[128 * kPitch];
+  const int64_t col_tiles = (rest_k + kTileCols - 1) / kTileCols;
+  const int64_t row_words = rest_k;  // K/16 bytes per plain row = rest_k 4-byte words
+  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+    const int64_t ct = t % col_tiles;
+    const int64_t mb = (t / col_tiles) % rest_m;
+    const int64_t l = t / (col_tiles * rest_m);
+    const int64_t col0 = ct * kTileCols;
+    const int ncols = (int)(rest_k - col0 < kTileCols ? rest_k - col0 : kTileCols);
+#pragma unroll
+    for (int w = threadIdx.x; w < kTileWords; w += kRepackThreads) {
+      const int r = w / kTileCols, cidx = w % kTileCols;
+      const int64_t m = mb * 128 + r;
+      uint32_t v = 0;
+      if (m < rows && cidx < ncols) v = src[(l * rows + m) * row_words + col0 + cidx];
+      tile[r * kPitch + cidx] = v;
+    }
+    __syncthreads();
+    // one 16-byte output vector = rows i, 32+i, 64+i, 96+i of one atom column
+    for (int v = threadIdx.x; v < 32 * kTileCols; v += kRepackThreads) {
+      const int cidx = v / 32, i = v % 32;
+      if (cidx < ncols) {
+        uint4 o;
+        o.x = tile[(i)*kPitch + cidx];
+        o.y = tile[(32 + i) * kPitch + cidx];
+        o.z = tile[(64 + i) * kPitch + cidx];
+        o.w = tile[(96 + i) * kPitch + cidx];
+        dst[((l * rest_m + mb) * rest_k + col0 + cidx) * 32 + i] = o;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t repack_ctas_per_sm(int* out) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, repack_scales_kernel, kRepackThreads,
+                                                       0);
+}
+
+cudaError_t launch_repack(const uint8_t* src, uint8_t* dst, int64_t rows, int64_t K, int64_t L,
+                          int64_t max_ctas, cudaStream_t stream) {
+  const int32_t rest_m = (int32_t)((rows + 127) / 128);
+  const int32_t rest_k = (int32_t)(K / 64);
+  const int64_t tiles = L * rest_m * ((rest_k + kTileCols - 1) / kTileCols);
+  if (tiles == 0) return cudaSuccess;
+  const int64_t cap = max_ctas > 0 ? max_ctas : 1;
+  const int64_t grid = tiles < cap ? tiles : cap;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kRepackThreads, 1, 1);
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, repack_scales_kernel, reinterpret_cast<const uint32_t*>(src),
+                            reinterpret_cast<uint4*>(dst), rows, rest_m, rest_k, tiles);
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,186 @@
+"""C ABI on the host (CPU only, no kernel launches).
+
+The library loads and exports every function the header declares; argument
+validation rejects bad calls before touching the GPU; the launch planner
+and the kernel's row partition are checked as host arithmetic.
+"""
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import nvfp4_block_scaled_gemv_gb300 as nv
+from nvfp4_block_scaled_gemv_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4_gemv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return nv.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declarations_match_binding_and_exports(lib):
+    declared = declared_functions()
+    assert declared == sorted(nv.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", nv.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(nvfp4_\w+)", out))
+    assert set(declared) <= exported
+
+
+def test_header_compiles_as_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "nvfp4_gemv.h"\nint main(void){return (int)NVFP4_OK;}\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), "-c",
+                    str(src), "-o", str(tmp_path / "t.o")], check=True)
+
+
+def _call(lib, a=64, b=64, sfa=64, sfb=64, c=64, M=8, K=64, L=1, layout=0):
+    return lib.nvfp4_gemv(a, b, sfa, sfb, c, M, K, L, layout, None)
+
+
+def test_validation_before_any_cuda_call(lib):
+    # the pointers below are never dereferenced: every case fails validation
+    assert _call(lib, M=-1) == nv.ERR_INVALID_VALUE
+    assert _call(lib, K=-64) == nv.ERR_INVALID_VALUE
+    assert _call(lib, L=-2) == nv.ERR_INVALID_VALUE
+    assert _call(lib, layout=2) == nv.ERR_INVALID_VALUE
+    assert _call(lib, K=96) == nv.ERR_UNSUPPORTED_SHAPE
+    assert _call(lib, K=(1 << 30) + 64) == nv.ERR_UNSUPPORTED_SHAPE
+    assert _call(lib, M=1 << 31) == nv.ERR_UNSUPPORTED_SHAPE
+    assert _call(lib, M=1 << 30, L=1 << 11) == nv.ERR_UNSUPPORTED_SHAPE
+    assert _call(lib, a=None) == nv.ERR_INVALID_VALUE
+    assert _call(lib, c=None) == nv.ERR_INVALID_VALUE
+    assert _call(lib, sfb=None) == nv.ERR_INVALID_VALUE
+    assert _call(lib, a=64 + 16) == nv.ERR_MISALIGNED
+    assert _call(lib, b=64 + 8) == nv.ERR_MISALIGNED
+    assert _call(lib, sfa=64 + 4) == nv.ERR_MISALIGNED
+    assert _call(lib, sfb=64 + 1) == nv.ERR_MISALIGNED
+    assert _call(lib, c=64 + 1) == nv.ERR_MISALIGNED
+
+
+def test_empty_problems_are_noops(lib):
+    assert _call(lib, a=None, b=None, sfa=None, sfb=None, c=None, M=0) == nv.OK
+    assert _call(lib, a=None, b=None, sfa=None, sfb=None, c=None, L=0) == nv.OK
+    assert lib.nvfp4_repack_scales(None, None, 0, 64, 1, None) == nv.OK
+    assert lib.nvfp4_repack_scales(None, None, 5, 0, 1, None) == nv.OK
+
+
+def test_explicit_schedule_validation(lib):
+    args = (64, 64, 64, 64, 64, 8, 64, 1, 0)
+    assert lib.nvfp4_gemv_explicit(*args, 12, 1, 1, None) == nv.ERR_INVALID_VALUE
+    assert lib.nvfp4_gemv_explicit(*args, 32, 3, 1, None) == nv.ERR_INVALID_VALUE
+    assert lib.nvfp4_gemv_explicit(*args, 32, 1, 0, None) == nv.ERR_INVALID_VALUE
+    assert lib.nvfp4_gemv_explicit(*args, 32, 1, 1 << 31, None) == nv.ERR_INVALID_VALUE
+
+
+def test_repack_validation(lib):
+    assert lib.nvfp4_repack_scales(64, 64, -1, 64, 1, None) == nv.ERR_INVALID_VALUE
+    assert lib.nvfp4_repack_scales(64, 64, 4, 80, 1, None) == nv.ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_repack_scales(None, 64, 4, 64, 1, None) == nv.ERR_INVALID_VALUE
+    assert lib.nvfp4_repack_scales(66, 64, 4, 64, 1, None) == nv.ERR_MISALIGNED
+    assert lib.nvfp4_repack_scales(64, 72, 4, 64, 1, None) == nv.ERR_MISALIGNED
+
+
+def test_permuted_scale_bytes_and_status_strings(lib):
+    assert nv.nvfp4_permuted_scale_bytes(7168, 2048, 4) == 4 * 56 * 32 * 512
+    assert nv.nvfp4_permuted_scale_bytes(1, 16384, 1) == 256 * 512
+    assert nv.nvfp4_permuted_scale_bytes(129, 64, 2) == 2 * 2 * 1 * 512
+    assert nv.nvfp4_permuted_scale_bytes(5, 80, 1) == 0
+    assert nv.status_string(nv.OK) == "NVFP4_OK"
+    assert nv.status_string(nv.ERR_MISALIGNED) == "NVFP4_ERR_MISALIGNED"
+    assert nv.status_string(99) == "NVFP4_ERR_UNKNOWN"
+    assert nv.nvfp4_last_cuda_error() == 0
+
+
+@pytest.mark.parametrize("M,K,L,lpr,ks,ctas", [
+    (128, 256, 1, 4, 1, 16),
+    (7168, 2048, 4, 32, 1, 304),
+    (4096, 7168, 8, 16, 1, 304),
+    (7168, 16384, 1, 32, 4, 304),
+    (16384, 8192, 16, 32, 1, 304),
+])
+def test_plan_for_the_benchmark_shapes(lib, M, K, L, lpr, ks, ctas):
+    plan = nv.nvfp4_gemv_plan(M, K, L, nv.SF_PLAIN, num_sms=152, ctas_per_sm=2)
+    assert (plan["lanes_per_row"], plan["k_split"], plan["ctas"]) == (lpr, ks, ctas)
+    assert plan["steps"] == -(-(K // 64) // lpr)
+    assert plan == nv.nvfp4_gemv_plan(M, K, L, nv.SF_PERMUTED_128x4, 152, 2)
+
+
+def test_plan_invariants_on_random_shapes(lib):
+    rng = np.random.default_rng(0)
+    for _ in range(300):
+        M = int(rng.integers(1, 20000))
+        K = 64 * int(rng.integers(0, 300))
+        L = int(rng.integers(1, 20))
+        sms = int(rng.integers(1, 200))
+        plan = nv.nvfp4_gemv_plan(M, K, L, 0, sms, 2)
+        kch = K // 64
+        assert plan["lanes_per_row"] in (4, 8, 16, 32) and plan["k_split"] in (1, 2, 4, 8)
+        assert plan["steps"] * plan["lanes_per_row"] >= kch
+        assert (plan["steps"] - 1) * plan["lanes_per_row"] < max(kch, 1)
+        assert 1 <= plan["ctas"] <= 2 * sms
+        assert plan["k_split"] == 1 or plan["k_split"] <= plan["steps"]
+
+
+# --- a model of the kernel's row partition (same integer arithmetic) ---------
+
+def visited_row(rp, perm):
+    if not perm:
+        return rp
+    q = rp & 127
+    j, t = q >> 3, q & 7
+    return (rp & ~127) + 32 * (t >> 1) + 2 * j + (t & 1)
+
+
+def partition(M, L, ctas, ks, perm):
+    """Rows each (cta, row lane, pass) handles, as (l, m) pairs."""
+    rows_per_l = ((M + 127) // 128) * 128 if perm else M
+    T = rows_per_l * L
+    wr_count = 8 // ks
+    seen = []
+    for cta in range(ctas):
+        c0, c1 = T * cta // ctas, T * (cta + 1) // ctas
+        for wr in range(wr_count):
+            r, r_end = c0 + (c1 - c0) * wr // wr_count, c0 + (c1 - c0) * (wr + 1) // wr_count
+            while r < r_end:
+                l = r // rows_per_l
+                pass_end = min(r_end, r + 8, (l + 1) * rows_per_l)
+                for rho in range(pass_end - r):
+                    m = visited_row(r + rho - l * rows_per_l, perm)
+                    if m < M:
+                        seen.append((l, m))
+                r = pass_end
+    return seen
+
+
+@pytest.mark.parametrize("perm", [False, True])
+@pytest.mark.parametrize("M,L,ctas,ks", [(1, 1, 1, 1), (7, 3, 2, 2), (128, 1, 16, 1),
+                                         (200, 3, 37, 4), (129, 2, 304, 8), (1000, 5, 13, 1)])
+def test_row_partition_covers_every_row_once(M, L, ctas, ks, perm):
+    seen = partition(M, L, ctas, ks, perm)
+    assert sorted(seen) == [(l, m) for l in range(L) for m in range(M)]
+
+
+def test_permuted_visit_order_groups_scale_sectors():
+    for blk in range(3):
+        order = [visited_row(blk * 128 + q, True) for q in range(128)]
+        assert sorted(order) == list(range(blk * 128, blk * 128 + 128))
+        for g in range(16):
+            rows = order[8 * g: 8 * g + 8]
+            # offsets of the rows' scale words in the 512-byte atom share one 32-byte sector
+            offs = {((m % 32) * 16 + ((m // 32) % 4) * 4) // 32 for m in rows}
+            assert len(offs) == 1

@@ -1,0 +1,234 @@
+"""GPU parity of nvfp4_gemv against the CPU oracle, called through the C ABI.
+
+Small and ragged shapes are compared element by element; the full-size
+benchmark workloads, in the launch schedule the benchmark times, are
+compared on sampled outputs the oracle computes one by one.  Tolerance:
+|gpu - oracle| <= 1e-3 * sum|terms| + 1 fp16 ulp of the oracle value.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import nvfp4_block_scaled_gemv_gb300 as nv  # noqa: E402
+import oracle  # noqa: E402
+from nvfp4_block_scaled_gemv_gb300 import build as libbuild  # noqa: E402
+from nvfp4_block_scaled_gemv_gb300 import synthetic  # noqa: E402
+from oracle import parity  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+SENTINEL = -4096.0
+SENTINEL_BITS = int(np.array([SENTINEL], dtype=np.float16).view(np.uint16)[0])
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    libbuild.build()
+    nv.library()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def to_dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+
+
+def bits(c):
+    return c.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def device_problem(p, M, K, L, layout, via_gpu_repack=False):
+    a, b = to_dev(p["a"]), to_dev(p["b"])
+    if layout == nv.SF_PLAIN:
+        sfa, sfb = to_dev(p["sfa"]), to_dev(p["sfb"])
+    elif via_gpu_repack:
+        sfa = nv.repack_scales(to_dev(p["sfa"]))
+        sfb = nv.repack_scales(to_dev(p["sfb"].reshape(L, 1, K // 16)))
+    else:
+        sfa = to_dev(oracle.repack_scales(p["sfa"], M, K, L))
+        sfb = to_dev(oracle.repack_scales(p["sfb"].reshape(L, 1, K // 16), 1, K, L))
+    return a, b, sfa, sfb
+
+
+def run(p, M, K, L, layout=nv.SF_PLAIN, schedule=None, via_gpu_repack=False):
+    a, b, sfa, sfb = device_problem(p, M, K, L, layout, via_gpu_repack)
+    # sentinel-filled c with slack on both sides: nothing outside [0, L*M) may change
+    pad = 64
+    buf = torch.full((L * M + 2 * pad,), SENTINEL, dtype=torch.float16, device=DEV)
+    c = buf[pad:pad + L * M]
+    if schedule is None:
+        nv.nvfp4_gemv(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(), c.data_ptr(),
+                      M, K, L, layout, torch.cuda.current_stream().cuda_stream)
+    else:
+        lpr, ks, ctas = schedule
+        nv.nvfp4_gemv_explicit(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(),
+                               c.data_ptr(), M, K, L, layout, lpr, ks, ctas,
+                               torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    whole = bits(buf)
+    assert np.all(whole[:pad] == SENTINEL_BITS) and np.all(whole[pad + L * M:] == SENTINEL_BITS), \
+        "write outside c"
+    return whole[pad:pad + L * M].reshape(L, M)
+
+
+SMALL_SHAPES = [
+    (128, 256, 1),   # the smallest benchmark workload
+    (1, 64, 1), (7, 64, 2), (8, 128, 1), (9, 192, 3), (31, 320, 1), (33, 1024, 2),
+    (127, 2048, 1), (129, 448, 2), (200, 7168, 1), (256, 4096, 3), (1000, 64, 4),
+    (37, 16384, 1), (513, 1152, 2),
+]
+
+
+@pytest.mark.parametrize("layout", [nv.SF_PLAIN, nv.SF_PERMUTED_128x4])
+@pytest.mark.parametrize("M,K,L", SMALL_SHAPES)
+def test_parity_all_outputs(M, K, L, layout):
+    p = synthetic.make_problem(M, K, L, seed=M + K + L)
+    ref, sums, sumabs = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
+    got = run(p, M, K, L, layout)
+    parity.assert_parity(got, ref, sums, sumabs, f"M={M} K={K} L={L} layout={layout}")
+
+
+@pytest.mark.parametrize("lpr", [4, 8, 16, 32])
+@pytest.mark.parametrize("ks", [1, 2, 4, 8])
+def test_every_schedule(lpr, ks):
+    M, K, L = 150, 2560, 3
+    p = synthetic.make_problem(M, K, L, seed=lpr * 10 + ks)
+    ref, sums, sumabs = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
+    outs = []
+    for ctas in (1, 7, 64, 600):
+        for layout in (nv.SF_PLAIN, nv.SF_PERMUTED_128x4):
+            got = run(p, M, K, L, layout, schedule=(lpr, ks, ctas))
+            parity.assert_parity(got, ref, sums, sumabs, f"lpr={lpr} ks={ks} ctas={ctas}")
+            outs.append(got)
+    # the summation order depends only on (lpr, ks): grid size and layout change no bit
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+
+
+def _sample_indices(M, L, n, rng):
+    m = [0, M - 1, min(127, M - 1), min(128, M - 1), M // 2]
+    mi = np.concatenate([rng.integers(0, M, n), np.tile(m, L)])
+    li = np.concatenate([rng.integers(0, L, n), np.repeat(np.arange(L), len(m))])
+    return mi, li
+
+
+@pytest.mark.parametrize("name,M,K,L", synthetic.WORKLOADS[1:])
+def test_full_size_workloads_sampled(name, M, K, L):
+    p = synthetic.make_problem(M, K, L, seed=0)
+    rng = np.random.default_rng(1)
+    mi, li = _sample_indices(M, L, 3000, rng)
+    ref, sums, sumabs = oracle.gemv_at(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L, mi, li)
+    results = {}
+    for layout in (nv.SF_PLAIN, nv.SF_PERMUTED_128x4):
+        got = run(p, M, K, L, layout, via_gpu_repack=(layout == nv.SF_PERMUTED_128x4))
+        parity.assert_parity(got[li, mi], ref, sums, sumabs, f"{name} layout={layout}")
+        assert np.isfinite(parity.half_values(got)).all()
+        results[layout] = got
+    assert np.array_equal(results[nv.SF_PLAIN], results[nv.SF_PERMUTED_128x4])
+
+
+def test_hand_worked_golden_values(golden_dir):
+    with open(os.path.join(golden_dir, "hand_dots.json")) as f:
+        cases = json.load(f)["cases"]
+    for case in cases:
+        p = {"a": np.frombuffer(bytes.fromhex(case["a"]), np.uint8).reshape(1, 1, 32),
+             "b": np.frombuffer(bytes.fromhex(case["b"]), np.uint8).reshape(1, 32),
+             "sfa": np.frombuffer(bytes.fromhex(case["sfa"]), np.uint8).reshape(1, 1, 4),
+             "sfb": np.frombuffer(bytes.fromhex(case["sfb"]), np.uint8).reshape(1, 4)}
+        for layout in (nv.SF_PLAIN, nv.SF_PERMUTED_128x4):
+            got = float(parity.half_values(run(p, 1, 64, 1, layout))[0, 0])
+            want = float(case["expected"])
+            if math.isnan(want):
+                assert math.isnan(got), case["name"]
+            else:
+                assert got == want, (case["name"], layout, got, want)
+
+
+def test_sign_flip_and_scale_doubling_are_exact():
+    M, K, L = 300, 4096, 2
+    p = synthetic.make_problem(M, K, L, seed=21)
+    base = parity.half_values(run(p, M, K, L))
+    flipped = dict(p, b=p["b"] ^ 0x88)
+    assert np.array_equal(parity.half_values(run(flipped, M, K, L)), -base)
+    doubled = dict(p, sfb=p["sfb"] + 8)
+    assert np.array_equal(parity.half_values(run(doubled, M, K, L)), 2 * base)
+
+
+def test_extreme_codes_and_nan():
+    rng = np.random.default_rng(5)
+    M, K, L = 64, 512, 2
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    p = {"a": rng.integers(0, 256, (L, M, K // 2), dtype=np.uint8),
+         "b": rng.integers(0, 256, (L, K // 2), dtype=np.uint8),
+         "sfa": rng.choice(finite, (L, M, K // 16)),
+         "sfb": rng.choice(finite, (L, K // 16))}
+    p["sfa"][0, 3, 5] = 0x7F           # NaN scale on one row
+    p["sfb"][1, 2] = 0xFF              # NaN scale on every row of batch 1
+    p["a"][0, 10] = 0x77               # +6 everywhere
+    p["sfa"][0, 10] = 0x7E             # 448: overflows to +inf
+    ref, sums, sumabs = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
+    for layout in (nv.SF_PLAIN, nv.SF_PERMUTED_128x4):
+        got = run(p, M, K, L, layout)
+        parity.assert_parity(got, ref, sums, sumabs, f"extreme layout={layout}")
+        v = parity.half_values(got)
+        assert np.isnan(v[0, 3]) and np.isnan(v[1]).all()
+
+
+def test_zero_k_writes_zeros_and_empty_is_noop():
+    M, L = 100, 3
+    c = torch.full((L, M), 7.0, dtype=torch.float16, device=DEV)
+    nv.nvfp4_gemv(0, 0, 0, 0, c.data_ptr(), M, 0, L, nv.SF_PLAIN,
+                  torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert np.all(bits(c) == 0)
+    nv.nvfp4_gemv(0, 0, 0, 0, 0, 0, 128, L, nv.SF_PLAIN, 0)
+    nv.nvfp4_gemv(0, 0, 0, 0, 0, M, 128, 0, nv.SF_PLAIN, 0)
+
+
+def test_deterministic_run_to_run():
+    M, K, L = 7168, 2048, 4
+    p = synthetic.make_problem(M, K, L, seed=3)
+    a, b, sfa, sfb = device_problem(p, M, K, L, nv.SF_PLAIN)
+    outs = []
+    for _ in range(3):
+        c = nv.gemv(a.view(L, M, K // 2), b, sfa.view(L, M, K // 16), sfb)
+        torch.cuda.synchronize()
+        outs.append(bits(c))
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
+
+
+def test_misaligned_device_pointers_rejected_without_launch():
+    M, K, L = 16, 128, 1
+    buf = torch.zeros(4096, dtype=torch.uint8, device=DEV)
+    c = torch.full((M,), 3.0, dtype=torch.float16, device=DEV)
+    base = buf.data_ptr()
+    with pytest.raises(nv.Nvfp4Error) as e:
+        nv.nvfp4_gemv(base + 16, base + 1024, base + 2048, base + 3072, c.data_ptr(), M, K, L)
+    assert e.value.status == nv.ERR_MISALIGNED
+    torch.cuda.synchronize()
+    assert np.all(parity.half_values(bits(c)) == 3.0)
+
+
+def test_graph_capture_and_replay():
+    M, K, L = 512, 1024, 2
+    p = synthetic.make_problem(M, K, L, seed=8)
+    a, b, sfa, sfb = device_problem(p, M, K, L, nv.SF_PLAIN)
+    a, sfa = a.view(L, M, K // 2), sfa.view(L, M, K // 16)
+    c = torch.zeros((L, M), dtype=torch.float16, device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        nv.gemv(a, b, sfa, sfb, c)  # warm-up outside capture
+    torch.cuda.synchronize()
+    want = bits(c)
+    c.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        nv.gemv(a, b, sfa, sfb, c, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(c), want)

@@ -1,0 +1,58 @@
+"""GPU scale repack: bit-exact against the oracle's closed form, padding included."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import nvfp4_block_scaled_gemv_gb300 as nv  # noqa: E402
+import oracle  # noqa: E402
+from nvfp4_block_scaled_gemv_gb300 import build as libbuild  # noqa: E402
+from nvfp4_block_scaled_gemv_gb300 import synthetic  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    libbuild.build()
+    nv.library()
+
+
+def gpu_repack(src, rows, K, L):
+    n = nv.nvfp4_permuted_scale_bytes(rows, K, L)
+    pad = 512
+    buf = torch.full((n + 2 * pad,), 0xA5, dtype=torch.uint8, device=DEV)
+    dst = buf[pad:pad + n]
+    s = torch.from_numpy(np.ascontiguousarray(src)).to(DEV)
+    nv.nvfp4_repack_scales(s.data_ptr(), dst.data_ptr(), rows, K, L,
+                           torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    whole = buf.cpu().numpy()
+    assert np.all(whole[:pad] == 0xA5) and np.all(whole[pad + n:] == 0xA5), "write outside dst"
+    return whole[pad:pad + n]
+
+
+@pytest.mark.parametrize("rows,K,L", [
+    (1, 64, 1), (1, 16384, 4), (31, 128, 2), (128, 64, 1), (129, 1088, 3), (200, 7168, 2),
+    (1000, 2048, 1), (4096, 64, 2), (7168, 2048, 4), (7168, 16384, 1), (333, 4160, 5),
+])
+def test_repack_bit_exact(rows, K, L):
+    rng = np.random.default_rng(rows + K)
+    src = rng.integers(0, 256, (L, rows, K // 16), dtype=np.uint8)
+    assert np.array_equal(gpu_repack(src, rows, K, L), oracle.repack_scales(src, rows, K, L))
+
+
+def test_repack_full_size_scales():
+    # sfa of the largest benchmark workload: 16 batches of 16384 x 512 scale bytes
+    M, K, L = 16384, 8192, 16
+    src = synthetic.scale_bytes(2, L * M * (K // 16)).reshape(L, M, K // 16)
+    assert np.array_equal(gpu_repack(src, M, K, L), oracle.repack_scales(src, M, K, L))
+
+
+def test_repack_overwrites_stale_padding():
+    rows, K, L = 5, 256, 2
+    src = np.full((L, rows, K // 16), 0x38, dtype=np.uint8)
+    got = gpu_repack(src, rows, K, L)  # dst pre-filled with 0xA5 inside gpu_repack's buffer
+    assert np.array_equal(got, oracle.repack_scales(src, rows, K, L))
+    assert np.count_nonzero(got) == src.size
