@@ -57,6 +57,10 @@ def parse_args():
     ap.add_argument("--layout", choices=["plain", "permuted"], default="plain")
     ap.add_argument("--all-configs", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--workload", default=WORKLOAD[0],
+                    choices=[w[0] for w in synthetic.WORKLOADS])
+    ap.add_argument("--ncu", action="store_true",
+                    help="only run warmup+steps calls of --workload (for profiler captures)")
     return ap.parse_args()
 
 
@@ -379,11 +383,12 @@ def run_native(args):
     nv.library()
     stream = torch.cuda.Stream(device=dev)
 
-    name, M, K, L = WORKLOAD
+    name, M, K, L = next(w for w in synthetic.WORKLOADS if w[0] == args.workload)
     layout = nv.SF_PLAIN if args.layout == "plain" else nv.SF_PERMUTED_128x4
     p = synthetic.make_problem(M, K, L, seed=0)
-    prob = DeviceProblem(torch, nv, p, M, K, L, layout, dev, ROTATE_SETS)
     nbytes = synthetic.algorithmic_bytes(M, K, L)
+    sets = max(2, min(ROTATE_SETS, -(-400 * 2 ** 20 // nbytes)))
+    prob = DeviceProblem(torch, nv, p, M, K, L, layout, dev, sets)
 
     sampler = ClockSampler(gpu_id_for_smi(torch, local)) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
@@ -409,7 +414,7 @@ def run_native(args):
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "e2m1xe4m3->f32->f16", "data": "synthetic",
         "config": {"workload": name, "M": M, "K": K, "L": L, "scale_layout": args.layout,
-                   "l2": f"{ROTATE_SETS} rotating input sets, {ROTATE_SETS * nbytes / 1e6:.0f} MB "
+                   "l2": f"{sets} rotating input sets, {sets * nbytes / 1e6:.0f} MB "
                          "> 2x L2 (cold L2 every call)",
                    "launch": "CUDA graph of back-to-back nvfp4_gemv calls, PDL",
                    "bytes_per_call": nbytes, "schedule": plan},
@@ -449,9 +454,32 @@ def run_native(args):
                 torch.cuda.empty_cache()
 
 
+def run_profile_case(args):
+    """Plain calls of one workload, nothing else on the GPU but input upload."""
+    import torch
+
+    import nvfp4_block_scaled_gemv_gb300 as nv
+    from nvfp4_block_scaled_gemv_gb300 import build as libbuild
+
+    libbuild.build()
+    dev = torch.device("cuda", 0)
+    name, M, K, L = next(w for w in synthetic.WORKLOADS if w[0] == args.workload)
+    layout = nv.SF_PLAIN if args.layout == "plain" else nv.SF_PERMUTED_128x4
+    p = synthetic.make_problem(M, K, L, seed=0)
+    prob = DeviceProblem(torch, nv, p, M, K, L, layout, dev, 2)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    for i in range(args.warmup + args.steps):
+        prob.call(nv, i, stream.cuda_stream)
+    stream.synchronize()
+    print(f"profile case done: {name} {args.layout} {args.warmup}+{args.steps} calls")
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.ncu:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_native(args)

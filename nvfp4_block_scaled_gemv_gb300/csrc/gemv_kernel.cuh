@@ -62,12 +62,14 @@ __device__ __forceinline__ int64_t scale_chunk_stride() {
 // of 1/4 below 36 in magnitude and each half2 lane sums 8 of them, so both
 // halves are exact; their fp32 sum is exact too.
 __device__ __forceinline__ float block_dot(uint32_t w0, uint32_t w1, const uint32_t (&bh)[8]) {
+  uint32_t d0[4], d1[4];
+  e2m1x8_to_f16x2x4(w0, d0);
+  e2m1x8_to_f16x2x4(w1, d1);
   uint32_t h = 0;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t w = (j < 4 ? w0 : w1) >> (8 * (j & 3));
-    h = hfma2(e2m1x2_to_f16x2(w), bh[j], h);
-  }
+  for (int j = 0; j < 4; ++j) h = hfma2(d0[j], bh[j], h);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) h = hfma2(d1[j], bh[4 + j], h);
   return f16_lo_to_f32(h) + f16_hi_to_f32(h);
 }
 
@@ -169,9 +171,16 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
           uint32_t bh[8];
+          {
+            uint32_t lo[4], hi[4];
+            e2m1x8_to_f16x2x4(bw[2 * blk], lo);
+            e2m1x8_to_f16x2x4(bw[2 * blk + 1], hi);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            bh[j] = e2m1x2_to_f16x2(bw[2 * blk + (j >> 2)] >> (8 * (j & 3)));
+            for (int j = 0; j < 4; ++j) {
+              bh[j] = lo[j];
+              bh[4 + j] = hi[j];
+            }
+          }
           const float sb = scale_of(sbw, blk);
 #pragma unroll
           for (int i = 0; i < NI; ++i) {

@@ -31,13 +31,14 @@ __device__ __forceinline__ uint32_t ld_scale_32(const void* p) {
   return v;
 }
 
-// Two E2M1 codes (low byte of v: low nibble first) -> f16x2 (low half first).
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t v) {
-  uint32_t out;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(out)
-      : "r"(v));
-  return out;
+// Four packed bytes of E2M1 pairs -> four f16x2 (byte j -> out[j]).  The
+// word is split into byte registers first, so no shifts are needed.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
 }
 
 // Two E4M3 codes (low 16 bits of v) -> f16x2.  Exact; NaN stays NaN.
