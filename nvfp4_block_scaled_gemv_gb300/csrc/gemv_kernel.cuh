@@ -20,8 +20,9 @@
 // Arithmetic: A and b nibbles are decoded with cvt.rn.f16x2.e2m1x2 and
 // multiplied with fma.rn.f16x2; all products are multiples of 1/4 below 36
 // in magnitude and each half2 lane sums 8 of them, so every partial sum is
-// exact in fp16.  The two halves go to fp32, are added (exact) and scaled by
-// sfa*sfb (exact in fp32), then accumulated in fp32.  Lane partials are
+// exact in fp16.  The two halves times sfa go to fp32 exactly (two mixed
+// fp16 x fp16 + fp32 fmas), and one fp32 fma adds that times sfb (exact
+// product) to the accumulator.  Lane partials are
 // combined by a shuffle butterfly; the summation order depends only on
 // (K, LPR, KS), so results are reproducible and identical for both scale
 // layouts.
@@ -58,10 +59,10 @@ __device__ __forceinline__ int64_t scale_chunk_stride() {
 }
 
 // Dot product of one 16-element block of one row with the matching block of
-// b (bh: 8 half2 holding b's elements 2j, 2j+1): every product is a multiple
-// of 1/4 below 36 in magnitude and each half2 lane sums 8 of them, so both
-// halves are exact; their fp32 sum is exact too.
-__device__ __forceinline__ float block_dot(uint32_t w0, uint32_t w1, const uint32_t (&bh)[8]) {
+// b (bh: 8 half2 holding b's elements 2j, 2j+1), as an f16x2 pair of partial
+// sums: every product is a multiple of 1/4 below 36 in magnitude and each
+// half2 lane sums 8 of them, so both halves are exact.
+__device__ __forceinline__ uint32_t block_dot(uint32_t w0, uint32_t w1, const uint32_t (&bh)[8]) {
   uint32_t d0[4], d1[4];
   e2m1x8_to_f16x2x4(w0, d0);
   e2m1x8_to_f16x2x4(w1, d1);
@@ -70,7 +71,15 @@ __device__ __forceinline__ float block_dot(uint32_t w0, uint32_t w1, const uint3
   for (int j = 0; j < 4; ++j) h = hfma2(d0[j], bh[j], h);
 #pragma unroll
   for (int j = 0; j < 4; ++j) h = hfma2(d1[j], bh[4 + j], h);
-  return f16_lo_to_f32(h) + f16_hi_to_f32(h);
+  return h;
+}
+
+// acc + (block dot) * sfa * sfb: the dot's two halves times sfa exactly
+// (f16x2_sum_times; sfa is the HI or low half of the f16x2 sa2), then one fp32
+// fma with sfb (exact product, one rounding).
+template <bool HI>
+__device__ __forceinline__ float block_accumulate(uint32_t h, uint32_t sa2, float sb, float acc) {
+  return fmaf(f16x2_sum_times<HI>(h, sa2), sb, acc);
 }
 
 // E4M3 scale of block blk (0..3) of a 4-byte scale word, as fp32 (exact).
@@ -185,8 +194,10 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
 #pragma unroll
           for (int i = 0; i < NI; ++i) {
             if (valid[i]) {
-              const float d = block_dot(av[i][2 * blk], av[i][2 * blk + 1], bh);
-              acc[i] = fmaf(d, scale_of(sw[i], blk) * sb, acc[i]);
+              const uint32_t h = block_dot(av[i][2 * blk], av[i][2 * blk + 1], bh);
+              const uint32_t sa2 = e4m3x2_to_f16x2(sw[i] >> (16 * (blk >> 1)));
+              acc[i] = (blk & 1) ? block_accumulate<true>(h, sa2, sb, acc[i])
+                                 : block_accumulate<false>(h, sa2, sb, acc[i]);
             }
           }
         }

@@ -72,6 +72,27 @@ __device__ __forceinline__ float f16_hi_to_f32(uint32_t h) {
   return f;
 }
 
+// (h.lo + h.hi) * s exactly in fp32, where h holds two fp16 partial sums and
+// s is the low (HI = false) or high half of the f16x2 s2.  Both fused
+// multiply-adds take fp16 operands and an fp32 addend; with the partial sums
+// multiples of 1/4 below 2^10 and s an E4M3 value (4 significant bits), every
+// intermediate fits in 24 bits, so nothing rounds.
+template <bool HI>
+__device__ __forceinline__ float f16x2_sum_times(uint32_t h, uint32_t s2) {
+  float t;
+  if (HI)
+    asm("{\n\t.reg .b16 l, u, a, b;\n\tmov.b32 {l, u}, %1;\n\tmov.b32 {a, b}, %2;\n\t"
+        "fma.rn.f32.f16 %0, l, b, 0f00000000;\n\tfma.rn.f32.f16 %0, u, b, %0;\n\t}"
+        : "=f"(t)
+        : "r"(h), "r"(s2));
+  else
+    asm("{\n\t.reg .b16 l, u, a, b;\n\tmov.b32 {l, u}, %1;\n\tmov.b32 {a, b}, %2;\n\t"
+        "fma.rn.f32.f16 %0, l, a, 0f00000000;\n\tfma.rn.f32.f16 %0, u, a, %0;\n\t}"
+        : "=f"(t)
+        : "r"(h), "r"(s2));
+  return t;
+}
+
 // Programmatic dependent launch: block until the preceding grid on the
 // stream has completed and its writes are visible (a no-op when the launch
 // carries no programmatic dependency).
