@@ -90,19 +90,32 @@ nvfp4_status_t nvfp4_gemv(const void* a, const void* b, const void* sfa, const v
                           void* c, int64_t M, int64_t K, int64_t L, int sf_layout,
                           struct CUstream_st* stream);
 
+/* The two GEMV kernels (same arithmetic, different data movement). */
+typedef enum {
+  /* Warps load up to 8 rows' 32-byte K chunks straight into registers with
+   * 256-bit loads, then compute. */
+  NVFP4_KERNEL_DIRECT = 0,
+  /* Each lane copies its rows' chunks and scale words into a 3-slot
+   * per-warp shared-memory ring with cp.async, so every warp keeps two tasks
+   * in flight while it computes one.  The default for every K > 0; needs
+   * k_split no larger than the K steps, ceil(K/64 / lanes_per_row). */
+  NVFP4_KERNEL_PIPELINED = 1
+} nvfp4_kernel_t;
+
 /*
- * nvfp4_gemv with the launch schedule given instead of chosen (for tuning
- * and for testing every schedule; same arguments, rules and results
- * contract as nvfp4_gemv).  lanes_per_row in {4, 8, 16, 32}: lanes sharing a
- * row; k_split in {1, 2, 4, 8}: warps splitting a row's K range; ctas in
- * [1, 2^31): grid size.  The summation order, and so the last bits of c,
- * depend on (lanes_per_row, k_split); any valid schedule meets the accuracy
- * contract.  Invalid schedule values give NVFP4_ERR_INVALID_VALUE.
+ * nvfp4_gemv with the kernel and launch schedule given instead of chosen
+ * (for tuning and for testing every schedule; same arguments, rules and
+ * results contract as nvfp4_gemv).  kernel: nvfp4_kernel_t;
+ * lanes_per_row in {4, 8, 16, 32}: lanes sharing a row; k_split in
+ * {1, 2, 4, 8}: warps splitting a row's K range; ctas in [1, 2^31): grid size.
+ * The summation order, and so the last bits of c, depend on (kernel,
+ * lanes_per_row, k_split); any valid schedule meets the accuracy contract.
+ * Invalid schedule values give NVFP4_ERR_INVALID_VALUE.
  */
 nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa,
                                    const void* sfb, void* c, int64_t M, int64_t K, int64_t L,
-                                   int sf_layout, int lanes_per_row, int k_split, int64_t ctas,
-                                   struct CUstream_st* stream);
+                                   int sf_layout, int kernel, int lanes_per_row, int k_split,
+                                   int64_t ctas, struct CUstream_st* stream);
 
 /*
  * Scale repack: plain [L][rows][K/16] E4M3 -> the 128x4-atom pre-permuted
@@ -130,21 +143,24 @@ int nvfp4_last_cuda_error(void);
 
 /*
  * Launch plan of nvfp4_gemv, computed on the host only (no GPU needed), for
- * inspection and tests.  num_sms is the device's multiprocessor count and
+ * inspection and tests.  kernel = -1 gives the plan nvfp4_gemv uses, an
+ * nvfp4_kernel_t value that kernel's plan (NVFP4_ERR_UNSUPPORTED_SHAPE if it
+ * cannot run the shape).  num_sms is the device's multiprocessor count and
  * ctas_per_sm the number of the kernel's CTAs resident per SM (pass 0 to use
- * the compiled-in default).
+ * the compiled-in default of 2).
  */
 typedef struct {
+  int kernel;         /* nvfp4_kernel_t */
   int lanes_per_row;  /* lanes of a warp that share one row (32-byte K chunk each) */
   int k_split;        /* warps of a CTA that split one row's K range */
-  int rows_per_pass;  /* rows a warp reduces at once (<= 8) */
+  int rows_per_pass;  /* rows a warp reduces at once */
   int threads_per_cta;
   int64_t ctas;       /* grid size */
   int64_t steps;      /* K chunks per lane per row, ceil(K/64 / lanes_per_row) */
 } nvfp4_gemv_plan_t;
 
-nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, int num_sms,
-                               int ctas_per_sm, nvfp4_gemv_plan_t* out);
+nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, int kernel,
+                               int num_sms, int ctas_per_sm, nvfp4_gemv_plan_t* out);
 
 #ifdef __cplusplus
 }

@@ -51,8 +51,12 @@ class Nvfp4Error(RuntimeError):
         super().__init__(msg)
 
 
+KERNEL_DIRECT = 0
+KERNEL_PIPELINED = 1
+
+
 class _Plan(ctypes.Structure):
-    _fields_ = [("lanes_per_row", ctypes.c_int), ("k_split", ctypes.c_int),
+    _fields_ = [("kernel", ctypes.c_int), ("lanes_per_row", ctypes.c_int), ("k_split", ctypes.c_int),
                 ("rows_per_pass", ctypes.c_int), ("threads_per_cta", ctypes.c_int),
                 ("ctas", ctypes.c_int64), ("steps", ctypes.c_int64)]
 
@@ -72,7 +76,7 @@ def library() -> ctypes.CDLL:
     P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     lib.nvfp4_gemv.argtypes = [P, P, P, P, P, I64, I64, I64, I, P]
     lib.nvfp4_gemv.restype = I
-    lib.nvfp4_gemv_explicit.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, I, I64, P]
+    lib.nvfp4_gemv_explicit.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, I, I, I64, P]
     lib.nvfp4_gemv_explicit.restype = I
     lib.nvfp4_repack_scales.argtypes = [P, P, I64, I64, I64, P]
     lib.nvfp4_repack_scales.restype = I
@@ -82,7 +86,7 @@ def library() -> ctypes.CDLL:
     lib.nvfp4_status_string.restype = ctypes.c_char_p
     lib.nvfp4_last_cuda_error.argtypes = []
     lib.nvfp4_last_cuda_error.restype = I
-    lib.nvfp4_gemv_plan.argtypes = [I64, I64, I64, I, I, I, ctypes.POINTER(_Plan)]
+    lib.nvfp4_gemv_plan.argtypes = [I64, I64, I64, I, I, I, I, ctypes.POINTER(_Plan)]
     lib.nvfp4_gemv_plan.restype = I
     _lib = lib
     return lib
@@ -104,11 +108,12 @@ def nvfp4_gemv(a: int, b: int, sfa: int, sfb: int, c: int, M: int, K: int, L: in
 
 
 def nvfp4_gemv_explicit(a: int, b: int, sfa: int, sfb: int, c: int, M: int, K: int, L: int,
-                        sf_layout: int, lanes_per_row: int, k_split: int, ctas: int,
+                        sf_layout: int, kernel: int, lanes_per_row: int, k_split: int, ctas: int,
                         stream: int = 0) -> None:
-    """nvfp4_gemv with an explicit launch schedule."""
-    _check(library().nvfp4_gemv_explicit(a, b, sfa, sfb, c, M, K, L, sf_layout, lanes_per_row,
-                                         k_split, ctas, stream), "nvfp4_gemv_explicit")
+    """nvfp4_gemv with an explicit kernel and launch schedule."""
+    _check(library().nvfp4_gemv_explicit(a, b, sfa, sfb, c, M, K, L, sf_layout, kernel,
+                                         lanes_per_row, k_split, ctas, stream),
+           "nvfp4_gemv_explicit")
 
 
 def nvfp4_repack_scales(src: int, dst: int, rows: int, K: int, L: int, stream: int = 0) -> None:
@@ -125,10 +130,11 @@ def nvfp4_last_cuda_error() -> int:
 
 
 def nvfp4_gemv_plan(M: int, K: int, L: int, sf_layout: int = SF_PLAIN, num_sms: int = 152,
-                    ctas_per_sm: int = 0) -> dict:
-    """The launch schedule nvfp4_gemv would use (host only, no GPU)."""
+                    ctas_per_sm: int = 0, kernel: int = -1) -> dict:
+    """The launch schedule nvfp4_gemv would use (kernel=-1) or one kernel's
+    schedule (host only, no GPU)."""
     plan = _Plan()
-    _check(library().nvfp4_gemv_plan(M, K, L, sf_layout, num_sms, ctas_per_sm,
+    _check(library().nvfp4_gemv_plan(M, K, L, sf_layout, kernel, num_sms, ctas_per_sm,
                                      ctypes.byref(plan)), "nvfp4_gemv_plan")
     return {name: getattr(plan, name) for name, _ in _Plan._fields_}
 

@@ -103,24 +103,39 @@ nvfp4_status_t run_gemv(const void* a, const void* b, const void* sfa, const voi
                         cudaStream_t stream) {
   const bool permuted = sf_layout == NVFP4_SF_PERMUTED_128x4;
   const GemvParams p = make_params(a, b, sfa, sfb, c, M, K, L, permuted, plan);
-  cudaError_t err = permuted ? launch_gemv_permuted(p, plan, stream)
-                             : launch_gemv_plain(p, plan, stream);
+  cudaError_t err;
+  if (plan.kernel == kKernelAsync)
+    err = permuted ? launch_async_permuted(p, plan, stream) : launch_async_plain(p, plan, stream);
+  else
+    err = permuted ? launch_gemv_permuted(p, plan, stream) : launch_gemv_plain(p, plan, stream);
   if (err != cudaSuccess) return cuda_failure(err);
   return NVFP4_OK;
 }
 
 }  // namespace
 
-// The schedule (see gemv_kernel.cuh for what each knob means):
+int rows_per_pass(int kernel, int lanes_per_row) {
+  return kernel == kKernelAsync ? kAsyncItems * (32 / lanes_per_row) : kRowsPerPass;
+}
+
+// The schedule (see gemv_kernel.cuh and gemv_async.cuh for what each knob
+// means):
+//  * kernel: the pipelined (cp.async) kernel for every K > 0; the direct
+//    kernel writes the zeros of K == 0;
 //  * lanes_per_row: the width among 32/16/8/4 lanes that leaves the fewest
 //    idle lane slots over K/64 chunks (ties go to the wider one);
 //  * ctas: one wave of resident CTAs (SMs x occupancy), fewer for tiny
 //    problems (at least 8 rows per CTA);
 //  * k_split: the smallest split that still gives each row lane of 8/k_split
-//    warps a full pass of 8 rows, capped by the number of chunk steps.
-bool plan_gemv(int64_t M, int64_t K, int64_t L, int num_sms, int ctas_per_sm, GemvPlan* out) {
+//    warps a full pass of rows, capped by the number of chunk steps (so that
+//    every K-split warp has a step in every pass).
+bool plan_gemv(int64_t M, int64_t K, int64_t L, int kernel, int num_sms, int ctas_per_sm,
+               GemvPlan* out) {
   if (M < 0 || K < 0 || L < 0 || num_sms < 1 || ctas_per_sm < 1 || out == nullptr) return false;
+  if (kernel < -1 || kernel > kKernelAsync) return false;
   const int64_t kchunks = K / 64;
+  if (kernel == -1) kernel = kchunks > 0 ? kKernelAsync : kKernelDirect;
+  if (kernel == kKernelAsync && kchunks == 0) return false;
   int lpr = 32;
   int64_t best_slots = -1;
   for (int cand : {32, 16, 8, 4}) {
@@ -132,13 +147,14 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, int num_sms, int ctas_per_sm, Ge
   }
   const int64_t steps = (kchunks + lpr - 1) / lpr;
   const int64_t rows = M * L;
+  const int64_t nr = rows_per_pass(kernel, lpr);
   int64_t ctas = (int64_t)num_sms * ctas_per_sm;
   const int64_t by_rows = (rows + kRowsPerPass - 1) / kRowsPerPass;
   if (by_rows < ctas) ctas = by_rows;
   if (ctas < 1) ctas = 1;
   int ks = 1;
-  while (ks < kGemvWarps && 2 * ks <= steps && rows * ks < ctas * kGemvWarps * kRowsPerPass)
-    ks *= 2;
+  while (ks < kGemvWarps && 2 * ks <= steps && rows * ks < ctas * kGemvWarps * nr) ks *= 2;
+  out->kernel = kernel;
   out->lanes_per_row = lpr;
   out->k_split = ks;
   out->ctas = ctas;
@@ -164,28 +180,33 @@ nvfp4_status_t nvfp4_gemv(const void* a, const void* b, const void* sfa, const v
   cudaError_t err = device_info(&sms, &occ, nullptr);
   if (err != cudaSuccess) return cuda_failure(err);
   GemvPlan plan;
-  if (!plan_gemv(M, K, L, sms, occ, &plan)) return NVFP4_ERR_INVALID_VALUE;
+  if (!plan_gemv(M, K, L, -1, sms, occ, &plan)) return NVFP4_ERR_INVALID_VALUE;
   return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, (cudaStream_t)stream);
 }
 
 nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa,
                                    const void* sfb, void* c, int64_t M, int64_t K, int64_t L,
-                                   int sf_layout, int lanes_per_row, int k_split, int64_t ctas,
-                                   struct CUstream_st* stream) {
+                                   int sf_layout, int kernel, int lanes_per_row, int k_split,
+                                   int64_t ctas, struct CUstream_st* stream) {
   nvfp4_status_t st = validate_gemv_shape(M, K, L, sf_layout);
   if (st != NVFP4_OK) return st;
+  if (kernel != kKernelDirect && kernel != kKernelAsync) return NVFP4_ERR_INVALID_VALUE;
   if (lanes_per_row != 4 && lanes_per_row != 8 && lanes_per_row != 16 && lanes_per_row != 32)
     return NVFP4_ERR_INVALID_VALUE;
   if (k_split != 1 && k_split != 2 && k_split != 4 && k_split != 8) return NVFP4_ERR_INVALID_VALUE;
   if (ctas < 1 || ctas > 0x7fffffff) return NVFP4_ERR_INVALID_VALUE;
+  const int64_t steps = (K / 64 + lanes_per_row - 1) / lanes_per_row;
+  // the pipelined kernel needs a K range and a step for every K-split warp
+  if (kernel == kKernelAsync && (K == 0 || k_split > steps)) return NVFP4_ERR_INVALID_VALUE;
   if (M == 0 || L == 0) return NVFP4_OK;
   st = validate_gemv_pointers(a, b, sfa, sfb, c, K);
   if (st != NVFP4_OK) return st;
   GemvPlan plan;
+  plan.kernel = kernel;
   plan.lanes_per_row = lanes_per_row;
   plan.k_split = k_split;
   plan.ctas = ctas;
-  plan.steps = (K / 64 + lanes_per_row - 1) / lanes_per_row;
+  plan.steps = steps;
   return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, (cudaStream_t)stream);
 }
 
@@ -225,17 +246,20 @@ const char* nvfp4_status_string(int status) {
 
 int nvfp4_last_cuda_error(void) { return g_last_cuda_error; }
 
-nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, int num_sms,
-                               int ctas_per_sm, nvfp4_gemv_plan_t* out) {
+nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, int kernel,
+                               int num_sms, int ctas_per_sm, nvfp4_gemv_plan_t* out) {
   if (out == nullptr || num_sms < 1 || ctas_per_sm < 0) return NVFP4_ERR_INVALID_VALUE;
   nvfp4_status_t st = validate_gemv_shape(M, K, L, sf_layout);
   if (st != NVFP4_OK) return st;
   GemvPlan plan;
-  if (!plan_gemv(M, K, L, num_sms, ctas_per_sm > 0 ? ctas_per_sm : kGemvMinCtasPerSm, &plan))
-    return NVFP4_ERR_INVALID_VALUE;
+  if (kernel < -1 || kernel > kKernelAsync) return NVFP4_ERR_INVALID_VALUE;
+  if (!plan_gemv(M, K, L, kernel, num_sms, ctas_per_sm > 0 ? ctas_per_sm : kGemvMinCtasPerSm,
+                 &plan))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  out->kernel = plan.kernel;
   out->lanes_per_row = plan.lanes_per_row;
   out->k_split = plan.k_split;
-  out->rows_per_pass = kRowsPerPass;
+  out->rows_per_pass = rows_per_pass(plan.kernel, plan.lanes_per_row);
   out->threads_per_cta = kGemvThreads;
   out->ctas = plan.ctas;
   out->steps = plan.steps;

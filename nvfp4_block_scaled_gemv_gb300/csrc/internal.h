@@ -9,7 +9,17 @@ namespace nvfp4 {
 constexpr int kGemvThreads = 256;   // 8 warps per CTA
 constexpr int kGemvWarps = kGemvThreads / 32;
 constexpr int kGemvMinCtasPerSm = 2;  // __launch_bounds__ occupancy floor
-constexpr int kRowsPerPass = 8;     // rows one warp reduces at once
+constexpr int kRowsPerPass = 8;     // rows one warp reduces at once (direct kernel)
+
+// Pipelined (cp.async) kernel: row items per lane per task, ring slots per
+// warp, and the per-warp slot size (A chunks [item][lane][32 B], then scale
+// words [item][lane][4 B]).
+constexpr int kAsyncItems = 4;
+constexpr int kAsyncStages = 3;
+constexpr int kAsyncStageBytes = kAsyncItems * (32 * 32 + 32 * 4);
+constexpr int kAsyncSmemBytes = kGemvWarps * kAsyncStages * kAsyncStageBytes;
+
+enum KernelKind { kKernelDirect = 0, kKernelAsync = 1 };
 
 // Everything a GEMV kernel needs, by value (kernel parameter space).
 struct GemvParams {
@@ -30,15 +40,20 @@ struct GemvParams {
 };
 
 struct GemvPlan {
+  int kernel;         // KernelKind
   int lanes_per_row;  // 4, 8, 16 or 32
   int k_split;        // 1, 2, 4 or 8 warps per row range
   int64_t ctas;
   int64_t steps;
 };
 
-// Host-only schedule choice (no CUDA calls).  Returns false for shapes the
-// planner cannot handle (caller validates first).
-bool plan_gemv(int64_t M, int64_t K, int64_t L, int num_sms, int ctas_per_sm, GemvPlan* out);
+// Host-only schedule choice (no CUDA calls) for one kernel, or for the
+// kernel the library picks (kernel = -1).  Returns false if the kernel cannot
+// run the shape (caller validates the shape first).
+bool plan_gemv(int64_t M, int64_t K, int64_t L, int kernel, int num_sms, int ctas_per_sm,
+               GemvPlan* out);
+// Rows one warp reduces at once in a kernel with a lane width.
+int rows_per_pass(int kernel, int lanes_per_row);
 
 // Occupancy of the GEMV kernel family on the current device (CTAs per SM).
 cudaError_t gemv_ctas_per_sm(int* out);
@@ -51,5 +66,7 @@ cudaError_t launch_repack(const uint8_t* src, uint8_t* dst, int64_t rows, int64_
 // Per-layout GEMV launchers (gemv_plain.cu, gemv_permuted.cu).
 cudaError_t launch_gemv_plain(const GemvParams& p, const GemvPlan& plan, cudaStream_t stream);
 cudaError_t launch_gemv_permuted(const GemvParams& p, const GemvPlan& plan, cudaStream_t stream);
+cudaError_t launch_async_plain(const GemvParams& p, const GemvPlan& plan, cudaStream_t stream);
+cudaError_t launch_async_permuted(const GemvParams& p, const GemvPlan& plan, cudaStream_t stream);
 
 }  // namespace nvfp4

@@ -93,6 +93,28 @@ __device__ __forceinline__ float f16x2_sum_times(uint32_t h, uint32_t s2) {
   return t;
 }
 
+// Per-thread asynchronous copies global -> shared (completion tracked per
+// thread with commit/wait groups).  16-byte copies bypass L1 (streamed data);
+// 4-byte copies go through L1 (scale words whose 32-byte sectors neighbouring
+// rows share).  Addresses must be aligned to the copy size.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
 // Programmatic dependent launch: block until the preceding grid on the
 // stream has completed and its writes are visible (a no-op when the launch
 // carries no programmatic dependency).

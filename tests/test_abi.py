@@ -81,10 +81,16 @@ def test_empty_problems_are_noops(lib):
 
 def test_explicit_schedule_validation(lib):
     args = (64, 64, 64, 64, 64, 8, 64, 1, 0)
-    assert lib.nvfp4_gemv_explicit(*args, 12, 1, 1, None) == nv.ERR_INVALID_VALUE
-    assert lib.nvfp4_gemv_explicit(*args, 32, 3, 1, None) == nv.ERR_INVALID_VALUE
-    assert lib.nvfp4_gemv_explicit(*args, 32, 1, 0, None) == nv.ERR_INVALID_VALUE
-    assert lib.nvfp4_gemv_explicit(*args, 32, 1, 1 << 31, None) == nv.ERR_INVALID_VALUE
+    for kernel in (nv.KERNEL_DIRECT, nv.KERNEL_PIPELINED):
+        assert lib.nvfp4_gemv_explicit(*args, kernel, 12, 1, 1, None) == nv.ERR_INVALID_VALUE
+        assert lib.nvfp4_gemv_explicit(*args, kernel, 32, 3, 1, None) == nv.ERR_INVALID_VALUE
+        assert lib.nvfp4_gemv_explicit(*args, kernel, 32, 1, 0, None) == nv.ERR_INVALID_VALUE
+        assert lib.nvfp4_gemv_explicit(*args, kernel, 32, 1, 1 << 31, None) == nv.ERR_INVALID_VALUE
+    assert lib.nvfp4_gemv_explicit(*args, 7, 32, 1, 1, None) == nv.ERR_INVALID_VALUE
+    # the pipelined kernel needs K > 0 and a K step for every K-split warp (K=64: one step)
+    assert lib.nvfp4_gemv_explicit(*args, nv.KERNEL_PIPELINED, 32, 2, 1, None) == nv.ERR_INVALID_VALUE
+    zero_k = (64, 64, 64, 64, 64, 8, 0, 1, 0)
+    assert lib.nvfp4_gemv_explicit(*zero_k, nv.KERNEL_PIPELINED, 32, 1, 1, None) == nv.ERR_INVALID_VALUE
 
 
 def test_repack_validation(lib):
@@ -106,18 +112,39 @@ def test_permuted_scale_bytes_and_status_strings(lib):
     assert nv.nvfp4_last_cuda_error() == 0
 
 
-@pytest.mark.parametrize("M,K,L,lpr,ks,ctas", [
-    (128, 256, 1, 4, 1, 16),
-    (7168, 2048, 4, 32, 1, 304),
-    (4096, 7168, 8, 16, 1, 304),
-    (7168, 16384, 1, 32, 4, 304),
-    (16384, 8192, 16, 32, 1, 304),
+BENCH_SHAPES = [(128, 256, 1), (7168, 2048, 4), (4096, 7168, 8), (7168, 16384, 1),
+                (16384, 8192, 16)]
+
+
+@pytest.mark.parametrize("shape,kernel,want", [
+    (BENCH_SHAPES[0], -1, (1, 4, 1, 16, 32)),
+    (BENCH_SHAPES[1], -1, (1, 32, 1, 304, 4)),
+    (BENCH_SHAPES[2], -1, (1, 16, 1, 304, 8)),
+    (BENCH_SHAPES[3], -1, (1, 32, 2, 304, 4)),
+    (BENCH_SHAPES[4], -1, (1, 32, 1, 304, 4)),
+    (BENCH_SHAPES[0], 0, (0, 4, 1, 16, 8)),
+    (BENCH_SHAPES[1], 0, (0, 32, 1, 304, 8)),
+    (BENCH_SHAPES[2], 0, (0, 16, 1, 304, 8)),
+    (BENCH_SHAPES[3], 0, (0, 32, 4, 304, 8)),
+    (BENCH_SHAPES[4], 0, (0, 32, 1, 304, 8)),
 ])
-def test_plan_for_the_benchmark_shapes(lib, M, K, L, lpr, ks, ctas):
-    plan = nv.nvfp4_gemv_plan(M, K, L, nv.SF_PLAIN, num_sms=152, ctas_per_sm=2)
-    assert (plan["lanes_per_row"], plan["k_split"], plan["ctas"]) == (lpr, ks, ctas)
-    assert plan["steps"] == -(-(K // 64) // lpr)
-    assert plan == nv.nvfp4_gemv_plan(M, K, L, nv.SF_PERMUTED_128x4, 152, 2)
+def test_plan_for_the_benchmark_shapes(lib, shape, kernel, want):
+    M, K, L = shape
+    plan = nv.nvfp4_gemv_plan(M, K, L, nv.SF_PLAIN, num_sms=152, ctas_per_sm=2, kernel=kernel)
+    got = tuple(plan[k] for k in ("kernel", "lanes_per_row", "k_split", "ctas", "rows_per_pass"))
+    assert got == want
+    assert plan["steps"] == -(-(K // 64) // plan["lanes_per_row"])
+    assert plan == nv.nvfp4_gemv_plan(M, K, L, nv.SF_PERMUTED_128x4, 152, 2, kernel=kernel)
+
+
+def test_kernel_choice(lib):
+    assert nv.nvfp4_gemv_plan(100, 0, 3, 0, 152, 2)["kernel"] == nv.KERNEL_DIRECT
+    assert nv.nvfp4_gemv_plan(100, 64, 3, 0, 152, 2)["kernel"] == nv.KERNEL_PIPELINED
+    with pytest.raises(nv.Nvfp4Error) as e:
+        nv.nvfp4_gemv_plan(100, 0, 3, 0, 152, 2, kernel=nv.KERNEL_PIPELINED)
+    assert e.value.status == nv.ERR_UNSUPPORTED_SHAPE
+    with pytest.raises(nv.Nvfp4Error):
+        nv.nvfp4_gemv_plan(100, 64, 3, 0, 152, 2, kernel=5)
 
 
 def test_plan_invariants_on_random_shapes(lib):
@@ -129,6 +156,7 @@ def test_plan_invariants_on_random_shapes(lib):
         sms = int(rng.integers(1, 200))
         plan = nv.nvfp4_gemv_plan(M, K, L, 0, sms, 2)
         kch = K // 64
+        assert plan["kernel"] == (nv.KERNEL_PIPELINED if kch else nv.KERNEL_DIRECT)
         assert plan["lanes_per_row"] in (4, 8, 16, 32) and plan["k_split"] in (1, 2, 4, 8)
         assert plan["steps"] * plan["lanes_per_row"] >= kch
         assert (plan["steps"] - 1) * plan["lanes_per_row"] < max(kch, 1)
@@ -146,8 +174,8 @@ def visited_row(rp, perm):
     return (rp & ~127) + 32 * (t >> 1) + 2 * j + (t & 1)
 
 
-def partition(M, L, ctas, ks, perm):
-    """Rows each (cta, row lane, pass) handles, as (l, m) pairs."""
+def partition(M, L, ctas, ks, perm, nr=8):
+    """Rows each (cta, row lane, pass of nr rows) handles, as (l, m) pairs."""
     rows_per_l = ((M + 127) // 128) * 128 if perm else M
     T = rows_per_l * L
     wr_count = 8 // ks
@@ -158,7 +186,7 @@ def partition(M, L, ctas, ks, perm):
             r, r_end = c0 + (c1 - c0) * wr // wr_count, c0 + (c1 - c0) * (wr + 1) // wr_count
             while r < r_end:
                 l = r // rows_per_l
-                pass_end = min(r_end, r + 8, (l + 1) * rows_per_l)
+                pass_end = min(r_end, r + nr, (l + 1) * rows_per_l)
                 for rho in range(pass_end - r):
                     m = visited_row(r + rho - l * rows_per_l, perm)
                     if m < M:
@@ -167,11 +195,12 @@ def partition(M, L, ctas, ks, perm):
     return seen
 
 
+@pytest.mark.parametrize("nr", [4, 8, 16, 32])
 @pytest.mark.parametrize("perm", [False, True])
 @pytest.mark.parametrize("M,L,ctas,ks", [(1, 1, 1, 1), (7, 3, 2, 2), (128, 1, 16, 1),
                                          (200, 3, 37, 4), (129, 2, 304, 8), (1000, 5, 13, 1)])
-def test_row_partition_covers_every_row_once(M, L, ctas, ks, perm):
-    seen = partition(M, L, ctas, ks, perm)
+def test_row_partition_covers_every_row_once(M, L, ctas, ks, perm, nr):
+    seen = partition(M, L, ctas, ks, perm, nr)
     assert sorted(seen) == [(l, m) for l in range(L) for m in range(M)]
 
 
@@ -184,3 +213,51 @@ def test_permuted_visit_order_groups_scale_sectors():
             # offsets of the rows' scale words in the 512-byte atom share one 32-byte sector
             offs = {((m % 32) * 16 + ((m // 32) % 4) * 4) // 32 for m in rows}
             assert len(offs) == 1
+
+
+def async_row(rp, perm, ri):
+    """Row order of the pipelined kernel (model of its integer arithmetic)."""
+    if not perm:
+        return rp
+    nr = 4 * ri
+    q = rp & 127
+    chunk, t = q // nr, q % nr
+    return (rp & ~127) + 32 * (t // ri) + chunk * ri + (t % ri)
+
+
+@pytest.mark.parametrize("ri", [1, 2, 4, 8])
+def test_pipelined_permuted_order_shares_scale_runs(ri):
+    nr = 4 * ri
+    for blk in range(2):
+        order = [async_row(blk * 128 + q, True, ri) for q in range(128)]
+        assert sorted(order) == list(range(blk * 128, blk * 128 + 128))
+        for c in range(128 // nr):
+            for sub in range(ri):
+                rows = [order[c * nr + g * ri + sub] for g in range(4)]  # a lane's 4 items
+                offs = [(m % 32) * 16 + ((m // 32) % 4) * 4 for m in rows]
+                assert offs == [offs[0] + 4 * g for g in range(4)] and offs[0] % 16 == 0
+
+
+@pytest.mark.parametrize("M,L,ctas,ks,ri", [(1, 1, 1, 1, 1), (129, 2, 37, 2, 2), (7168, 4, 304, 1, 1),
+                                            (1000, 3, 13, 4, 8), (200, 1, 600, 8, 4)])
+def test_pipelined_permuted_chunks_cover_every_row_once(M, L, ctas, ks, ri):
+    nr = 4 * ri
+    rows_per_l = ((M + 127) // 128) * 128
+    T = rows_per_l * L // nr
+    wr_count = 8 // ks
+    seen = []
+    for cta in range(ctas):
+        c0, c1 = T * cta // ctas, T * (cta + 1) // ctas
+        for wr in range(wr_count):
+            r = (c0 + (c1 - c0) * wr // wr_count) * nr
+            r_end = (c0 + (c1 - c0) * (wr + 1) // wr_count) * nr
+            while r < r_end:
+                l = r // rows_per_l
+                cnt = min(r_end, r + nr, (l + 1) * rows_per_l) - r
+                assert cnt == nr  # aligned chunks: every pass is one whole chunk
+                for rho in range(cnt):
+                    m = async_row(r - l * rows_per_l + rho, True, ri)
+                    if m < M:
+                        seen.append((l, m))
+                r += cnt
+    assert sorted(seen) == [(l, m) for l in range(L) for m in range(M)]

@@ -65,9 +65,9 @@ def run(p, M, K, L, layout=nv.SF_PLAIN, schedule=None, via_gpu_repack=False):
         nv.nvfp4_gemv(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(), c.data_ptr(),
                       M, K, L, layout, torch.cuda.current_stream().cuda_stream)
     else:
-        lpr, ks, ctas = schedule
+        kernel, lpr, ks, ctas = schedule
         nv.nvfp4_gemv_explicit(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(),
-                               c.data_ptr(), M, K, L, layout, lpr, ks, ctas,
+                               c.data_ptr(), M, K, L, layout, kernel, lpr, ks, ctas,
                                torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     whole = bits(buf)
@@ -93,19 +93,23 @@ def test_parity_all_outputs(M, K, L, layout):
     parity.assert_parity(got, ref, sums, sumabs, f"M={M} K={K} L={L} layout={layout}")
 
 
+@pytest.mark.parametrize("kernel", [nv.KERNEL_DIRECT, nv.KERNEL_PIPELINED])
 @pytest.mark.parametrize("lpr", [4, 8, 16, 32])
 @pytest.mark.parametrize("ks", [1, 2, 4, 8])
-def test_every_schedule(lpr, ks):
+def test_every_schedule(kernel, lpr, ks):
     M, K, L = 150, 2560, 3
+    if kernel == nv.KERNEL_PIPELINED and ks > -(-(K // 64) // lpr):
+        pytest.skip("the pipelined kernel needs a K step for every K-split warp")
     p = synthetic.make_problem(M, K, L, seed=lpr * 10 + ks)
     ref, sums, sumabs = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
     outs = []
     for ctas in (1, 7, 64, 600):
         for layout in (nv.SF_PLAIN, nv.SF_PERMUTED_128x4):
-            got = run(p, M, K, L, layout, schedule=(lpr, ks, ctas))
-            parity.assert_parity(got, ref, sums, sumabs, f"lpr={lpr} ks={ks} ctas={ctas}")
+            got = run(p, M, K, L, layout, schedule=(kernel, lpr, ks, ctas))
+            parity.assert_parity(got, ref, sums, sumabs,
+                                 f"kernel={kernel} lpr={lpr} ks={ks} ctas={ctas}")
             outs.append(got)
-    # the summation order depends only on (lpr, ks): grid size and layout change no bit
+    # the summation order depends only on (kernel, lpr, ks): grid and layout change no bit
     for o in outs[1:]:
         assert np.array_equal(o, outs[0])
 
