@@ -22,36 +22,6 @@
 
 namespace nvfp4 {
 
-// The (pass, K step) tasks of one warp: passes of up to NR rows of one batch
-// over the row lane's range and, in each pass, the steps ks, ks + KS, ...
-// below p.steps (the planner keeps KS <= steps, so every pass has one).
-template <int NR>
-struct TaskCursor {
-  int64_t r, l, end;
-  int cnt, s;
-  bool done;
-
-  __device__ __forceinline__ void start_pass(const GemvParams& p, int ks) {
-    done = r >= end;
-    if (done) return;
-    l = r / p.rows_per_l;
-    cnt = (int)(min(min(end, r + NR), (l + 1) * p.rows_per_l) - r);
-    s = ks;
-  }
-  __device__ __forceinline__ void init(const GemvParams& p, int64_t begin, int64_t e, int ks) {
-    r = begin;
-    end = e;
-    start_pass(p, ks);
-  }
-  __device__ __forceinline__ void advance(const GemvParams& p, int ks, int KS) {
-    s += KS;
-    if (s >= p.steps) {
-      r += cnt;
-      start_pass(p, ks);
-    }
-  }
-};
-
 // Row order of the pipelined kernel.  Plain scales: m = 0..M-1.  Permuted
 // scales: inside each 128-row atom block, pass c (NR = 4*RI rows) holds the
 // rows 32*g + c*RI + sub for g = 0..3 and sub < RI, in slot order g*RI + sub.
@@ -66,12 +36,84 @@ __device__ __forceinline__ int64_t async_row(int64_t rp) {
   return (rp & ~(int64_t)127) + 32 * (t / RI) + chunk * RI + (t % RI);
 }
 
+// The (pass, K step) tasks of one warp: passes of NR = NI*RI rows of one
+// batch over the row lane's range and, in each pass, the steps ks, ks + KS,
+// ... below p.steps (the planner keeps KS <= steps, so every pass has one).
+// What a lane needs per pass (pointers to its item-0 row of A, scales and
+// c, and which items are real rows) is computed once when the pass starts;
+// item i sits a fixed kernel-wide stride further, and a task adds only its K
+// offset.
+template <int LPR, bool PERM>
+struct TaskCursor {
+  static constexpr int NI = kAsyncItems, RI = 32 / LPR, NR = NI * RI;
+  static constexpr int ROW_STEP = PERM ? 32 : RI;  // rows between a lane's items
+  int64_t r, end;        // first visit-order row of the pass, end of the range
+  int64_t l_begin;       // first visit row of the pass's batch
+  int64_t l_end;         // first visit row of the next batch
+  int64_t lm;            // l * M
+  int l, cnt, s;
+  bool done;
+  uint32_t valid;        // bit i: the lane's item i is a real row
+  const uint8_t* a0;     // the lane's item-0 row of A
+  const uint8_t* s0;     // plain: its scale row; permuted: its 16-byte atom run (kt = 0)
+  int64_t c0;            // index of its item-0 output
+
+  __device__ __forceinline__ void start_pass(const GemvParams& p, int ks, int sub) {
+    done = r >= end;
+    if (done) return;
+    if (r >= l_end) {  // passes never cross a batch, and advance by at most one
+      ++l;
+      l_begin = l_end;
+      l_end += p.rows_per_l;
+      lm += p.M;
+    }
+    const int64_t left = min(end, l_end) - r;
+    cnt = left < NR ? (int)left : NR;
+    s = ks;
+    const int64_t rp = r - l_begin;  // visit row of the pass inside its batch
+    valid = 0;
+    if (!PERM) {
+      c0 = lm + rp + sub;
+      s0 = p.sfa + c0 * p.blocks;
+#pragma unroll
+      for (int i = 0; i < NI; ++i)
+        if (i * RI + sub < cnt) valid |= 1u << i;
+    } else {
+      const int64_t m0 = async_row<true, RI>(rp + sub);  // item i is row m0 + 32*i
+      c0 = lm + m0;
+      s0 = p.sfa + (((int64_t)l * p.rest_m + (m0 >> 7)) * p.rest_k) * 512 + (m0 & 31) * 16;
+#pragma unroll
+      for (int i = 0; i < NI; ++i)
+        if (i * RI + sub < cnt && m0 + 32 * i < p.M) valid |= 1u << i;
+    }
+    a0 = p.a + c0 * p.half_k;
+  }
+  __device__ __forceinline__ void init(const GemvParams& p, int64_t begin, int64_t e, int ks,
+                                       int sub) {
+    r = begin;
+    end = e;
+    l = (int)(begin < e ? begin / p.rows_per_l : 0);
+    l_begin = (int64_t)l * p.rows_per_l;
+    l_end = l_begin + p.rows_per_l;
+    lm = (int64_t)l * p.M;
+    start_pass(p, ks, sub);
+  }
+  __device__ __forceinline__ void advance(const GemvParams& p, int ks, int KS, int sub) {
+    s += KS;
+    if (s >= p.steps) {
+      r += cnt;
+      start_pass(p, ks, sub);
+    }
+  }
+};
+
 template <int LPR, int KS, bool PERM>
 __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
     nvfp4_gemv_async_kernel(const GemvParams p) {
-  constexpr int NI = kAsyncItems;          // row items per lane per task
-  constexpr int RI = 32 / LPR;             // rows per warp-wide item
-  constexpr int NR = NI * RI;              // rows per pass
+  using Cursor = TaskCursor<LPR, PERM>;
+  constexpr int NI = Cursor::NI;           // row items per lane per task
+  constexpr int RI = Cursor::RI;           // rows per warp-wide item
+  constexpr int NR = Cursor::NR;           // rows per pass
   constexpr int WR = kGemvWarps / KS;      // row lanes per CTA
   constexpr int S = kAsyncStages;
   constexpr int SFA_OFF = NI * 1024;       // scale words ([lane][item] words) follow the A chunks
@@ -107,79 +149,87 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
 
   pdl_wait();
 
+  const int64_t a_step = (int64_t)Cursor::ROW_STEP * p.half_k;
+  const int64_t s_step = (int64_t)Cursor::ROW_STEP * p.blocks;
+
   // copy this lane's part of task t (A chunks and scale words of its rows)
-  auto issue = [&](const TaskCursor<NR>& t, int slot) {
+  auto issue = [&](const Cursor& t, int slot) {
     const int kt = t.s * LPR + kc;
     if (kt >= p.kchunks) return;
     const uint32_t a_dst = ring + (uint32_t)(slot * kAsyncStageBytes + lane * 32);
     const uint32_t s_dst = ring + (uint32_t)(slot * kAsyncStageBytes + SFA_OFF + lane * 16);
-    const int64_t rp0 = t.r - t.l * p.rows_per_l;
+    const uint8_t* a_src = t.a0 + kt * 32;
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
-      const int rho = i * RI + sub;
-      if (rho < t.cnt) {
-        const int64_t m = async_row<PERM, RI>(rp0 + rho);
-        if (m < p.M) {
-          const uint8_t* src = p.a + (t.l * p.M + m) * p.half_k + (int64_t)kt * 32;
-          cp_async_16(a_dst + i * 1024, src);
-          cp_async_16(a_dst + i * 1024 + 16, src + 16);
-          if (!PERM) cp_async_4(s_dst + i * 4, p.sfa + (t.l * p.M + m) * p.blocks + kt * 4);
-        }
+      if (t.valid & (1u << i)) {
+        cp_async_16(a_dst + i * 1024, a_src + i * a_step);
+        cp_async_16(a_dst + i * 1024 + 16, a_src + i * a_step + 16);
+        if (!PERM) cp_async_4(s_dst + i * 4, t.s0 + kt * 4 + i * s_step);
       }
     }
-    if (PERM) {
-      // rows g = 0..3 of this lane: one 16-byte run of the atom (padding rows
-      // of the last block are in the atom too and read as 0x00)
-      const int64_t m0 = async_row<PERM, RI>(rp0 + sub);
-      cp_async_16(s_dst, p.sfa + ((t.l * p.rest_m + (m0 >> 7)) * p.rest_k + kt) * 512 +
-                             (m0 & 31) * 16);
-    }
+    // permuted: the four rows m0 + 32*i of this lane are one 16-byte run of
+    // the atom (padding rows of the last block included, read as 0x00)
+    if (PERM) cp_async_16(s_dst, t.s0 + (int64_t)kt * 512);
   };
-  auto load_b = [&](const TaskCursor<NR>& t, uint32_t (&w)[8], uint32_t& sw) {
-    const int kt = t.s * LPR + kc;
+  auto load_b = [&](int l, int kt, uint32_t (&w)[8], uint32_t& sw) {
     if (kt < p.kchunks) {
-      ld_shared_256(p.b + t.l * p.half_k + (int64_t)kt * 32, w);
-      sw = ld_scale_32(p.sfb + (PERM ? (t.l * p.rest_k + kt) * 512 : t.l * p.blocks + kt * 4));
+      ld_shared_256(p.b + (int64_t)l * p.half_k + kt * 32, w);
+      sw = ld_scale_32(p.sfb + (PERM ? ((int64_t)l * p.rest_k + kt) * 512
+                                     : (int64_t)l * p.blocks + kt * 4));
     }
   };
 
-  TaskCursor<NR> ld, cp;
-  ld.init(p, r_begin, r_end, ks);
+  Cursor ld, cp;
+  ld.init(p, r_begin, r_end, ks, sub);
   cp = ld;
 #pragma unroll
   for (int j = 0; j < S - 1; ++j) {
     if (!ld.done) {
       issue(ld, j);
-      ld.advance(p, ks, KS);
+      ld.advance(p, ks, KS, sub);
     }
     cp_async_commit();
   }
+  // b (and sfb) of the task being computed, and of the next one when it differs
+  uint32_t bw[8] = {0, 0, 0, 0, 0, 0, 0, 0}, sbw = 0;
   uint32_t bw_n[8] = {0, 0, 0, 0, 0, 0, 0, 0}, sbw_n = 0;
-  if (!cp.done) load_b(cp, bw_n, sbw_n);
+  if (!cp.done) load_b(cp.l, cp.s * LPR + kc, bw, sbw);
 
   float acc[NI];
 #pragma unroll
   for (int i = 0; i < NI; ++i) acc[i] = 0.f;
   int slot = 0;
+  bool pending_b = false;
 
   while (!cp.done) {
     // the slot computed in the previous iteration is free again
     if (!ld.done) {
       issue(ld, (slot + S - 1) % S);
-      ld.advance(p, ks, KS);
+      ld.advance(p, ks, KS, sub);
     }
     cp_async_commit();
-    uint32_t bw[8];
+    // the next task's b: same K step of the next pass, or the next step;
+    // it changes unless there is one step per row and the batch stays
+    const bool last_step = cp.s + KS >= p.steps;
+    const bool more = !last_step || cp.r + cp.cnt < cp.end;
+    const int s_n = last_step ? ks : cp.s + KS;
+    const int l_n = (last_step && cp.r + cp.cnt >= cp.l_end) ? cp.l + 1 : cp.l;
+    // b loaded during the previous task moves in only now, so its load
+    // latency is hidden behind a whole task's compute
+    if (pending_b) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) bw[j] = bw_n[j];
-    const uint32_t sbw = sbw_n;
-    TaskCursor<NR> nxt = cp;
-    nxt.advance(p, ks, KS);
-    if (!nxt.done) load_b(nxt, bw_n, sbw_n);
+      for (int j = 0; j < 8; ++j) bw[j] = bw_n[j];
+      sbw = sbw_n;
+      pending_b = false;
+    }
+    const bool new_b = more && (s_n != cp.s || l_n != cp.l);
+    if (new_b) {
+      load_b(l_n, s_n * LPR + kc, bw_n, sbw_n);
+      pending_b = true;
+    }
     cp_async_wait<S - 1>();
 
     const int kt = cp.s * LPR + kc;
-    const int64_t rp0 = cp.r - cp.l * p.rows_per_l;
     if (kt < p.kchunks) {
       // Lanes with bit 2 set process the chunk's second 16-byte half (blocks
       // 2, 3) first; their b words and scale bytes are rotated to match, so the
@@ -195,14 +245,9 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
         bwr[4 + j] = swp ? bw[j] : bw[4 + j];
       }
       const uint32_t sbwr = __funnelshift_l(sbw, sbw, rot16);
-      bool valid[NI];
       uint32_t saw[NI];
 #pragma unroll
-      for (int i = 0; i < NI; ++i) {
-        const int rho = i * RI + sub;
-        valid[i] = rho < cp.cnt && async_row<PERM, RI>(rp0 + rho) < p.M;
-        saw[i] = __funnelshift_l(sws[i], sws[i], rot16);
-      }
+      for (int i = 0; i < NI; ++i) saw[i] = __funnelshift_l(sws[i], sws[i], rot16);
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         uint32_t bh0[8], bh1[8];
@@ -224,7 +269,7 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
         const float sb0 = scale_of(sbwr, 2 * j), sb1 = scale_of(sbwr, 2 * j + 1);
 #pragma unroll
         for (int i = 0; i < NI; ++i) {
-          if (valid[i]) {
+          if (cp.valid & (1u << i)) {
             const uint4 x = *reinterpret_cast<const uint4*>(a_slot + i * 1024 + ((j * 16) ^ h0));
             const uint32_t sa2 = e4m3x2_to_f16x2(saw[i] >> (16 * j));
             acc[i] = block_accumulate<false>(block_dot(x.x, x.y, bh0), sa2, sb0, acc[i]);
@@ -234,8 +279,7 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
       }
     }
 
-    const bool pass_end = nxt.done || nxt.r != cp.r;
-    if (pass_end) {
+    if (last_step) {
       float v = lane_reduce<NI, LPR / 2>(acc, lane);
       const int rho_out = (kc / (LPR / NI)) * RI + sub;
       const bool holder = (kc % (LPR / NI)) == 0;
@@ -250,14 +294,15 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
         }
         named_barrier_sync(1 + wr, 32 * KS);
       }
-      if ((KS == 1 || ks == 0) && holder && rho_out < cp.cnt) {
-        const int64_t m = async_row<PERM, RI>(rp0 + rho_out);
-        if (m < p.M) p.c[cp.l * p.M + m] = __half_as_ushort(__float2half_rn(v));
-      }
+      // a holder keeps item rho_out / RI of its own lane group (rho_out % RI
+      // == sub), so its cursor knows the row
+      const int item = rho_out / RI;
+      if ((KS == 1 || ks == 0) && holder && (cp.valid & (1u << item)))
+        p.c[cp.c0 + item * Cursor::ROW_STEP] = __half_as_ushort(__float2half_rn(v));
 #pragma unroll
       for (int i = 0; i < NI; ++i) acc[i] = 0.f;
     }
-    cp = nxt;
+    cp.advance(p, ks, KS, sub);
     slot = (slot + 1 == S) ? 0 : slot + 1;
   }
   cp_async_wait<0>();
