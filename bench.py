@@ -234,8 +234,9 @@ def time_graph(torch, nv, prob, steps, warmup, stream):
     with torch.cuda.graph(graph, stream=stream):
         for i in range(g_size):
             prob.call(nv, i, handle)
-    for _ in range(2):
-        graph.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            graph.replay()
     stream.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
