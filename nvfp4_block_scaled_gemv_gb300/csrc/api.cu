@@ -95,6 +95,13 @@ GemvParams make_params(const void* a, const void* b, const void* sfa, const void
   p.blocks = (int32_t)(K / 16);
   p.kchunks = (int32_t)(K / 64);
   p.steps = (int32_t)plan.steps;
+  // rows per partition unit: the pipelined kernel hands permuted-scale rows
+  // out in aligned groups of its item rows, everything else row by row
+  const int64_t unit =
+      (plan.kernel == kKernelAsync && permuted) ? kAsyncItems * (32 / plan.lanes_per_row) : 1;
+  const int64_t units = p.rows_total / unit;
+  p.units_q = units / plan.ctas;
+  p.units_r = (int32_t)(units % plan.ctas);
   return p;
 }
 
@@ -114,51 +121,117 @@ nvfp4_status_t run_gemv(const void* a, const void* b, const void* sfa, const voi
 
 }  // namespace
 
-int rows_per_pass(int kernel, int lanes_per_row) {
-  return kernel == kKernelAsync ? kAsyncItems * (32 / lanes_per_row) : kRowsPerPass;
+int rows_per_pass(const GemvPlan& plan) {
+  return plan.kernel == kKernelAsync ? kAsyncItems * (32 / plan.lanes_per_row) * plan.groups
+                                     : kRowsPerPass;
+}
+
+namespace {
+
+// Rows of the longest row-lane range: CTA ranges differ by at most one unit
+// (a row, or an aligned group of rows for permuted scales) and a CTA's range
+// is cut evenly among its 8/k_split row lanes.
+int64_t max_rows_per_row_lane(int64_t M, int64_t L, bool permuted, int lanes_per_row,
+                              int k_split, int64_t ctas) {
+  const int64_t nr = kAsyncItems * (32 / lanes_per_row);
+  const int64_t unit = permuted ? nr : 1;
+  const int64_t rows_per_l = permuted ? (M + 127) / 128 * 128 : M;
+  const int64_t t = rows_per_l * L / unit;
+  const int64_t per_cta = (t + ctas - 1) / ctas;
+  const int64_t lanes = kGemvWarps / k_split;
+  return (per_cta + lanes - 1) / lanes * unit;
+}
+
+// Rough issue cost of the busiest warp under a pipelined schedule, in warp
+// instructions: item chunks (decode, dot, scale), tasks (copies, loop),
+// decoded b chunks, and per pass the lane reduction and store of each group
+// plus the K-split exchange.
+double async_cost(int64_t M, int64_t L, bool permuted, int64_t kchunks, int lpr, int ks,
+                  int64_t ctas, int groups) {
+  const int64_t ri = 32 / lpr, nr = kAsyncItems * ri;
+  const int64_t steps = (kchunks + lpr - 1) / lpr;
+  const int64_t steps_w = (steps + ks - 1) / ks;
+  const int64_t rows = max_rows_per_row_lane(M, L, permuted, lpr, ks, ctas);
+  const int64_t ngroups = (rows + nr - 1) / nr;
+  const int64_t passes = (ngroups + groups - 1) / groups;
+  const int64_t items = (rows + ri - 1) / ri;
+  const int64_t b_chunks = steps_w > 1 ? passes * steps_w : 1;
+  return 85.0 * items * steps_w + 45.0 * ngroups * steps_w + 45.0 * b_chunks +
+         passes * (50.0 + (ks > 1 ? 80.0 : 0.0)) + 25.0 * ngroups;
+}
+
+}  // namespace
+
+int async_groups(int64_t M, int64_t L, bool permuted, int lanes_per_row, int k_split,
+                 int64_t ctas) {
+  const int64_t nr = kAsyncItems * (32 / lanes_per_row);
+  const int64_t rows = max_rows_per_row_lane(M, L, permuted, lanes_per_row, k_split, ctas);
+  const int64_t g = (rows + nr - 1) / nr;
+  return g <= 1 ? 1 : g <= 2 ? 2 : 4;
 }
 
 // The schedule (see gemv_kernel.cuh and gemv_async.cuh for what each knob
 // means):
 //  * kernel: the pipelined (cp.async) kernel for every K > 0; the direct
 //    kernel writes the zeros of K == 0;
-//  * lanes_per_row: the width among 32/16/8/4 lanes that leaves the fewest
-//    idle lane slots over K/64 chunks (ties go to the wider one);
 //  * ctas: one wave of resident CTAs (SMs x occupancy), fewer for tiny
 //    problems (at least 8 rows per CTA);
-//  * k_split: the smallest split that still gives each row lane of 8/k_split
-//    warps a full pass of rows, capped by the number of chunk steps (so that
-//    every K-split warp has a step in every pass).
-bool plan_gemv(int64_t M, int64_t K, int64_t L, int kernel, int num_sms, int ctas_per_sm,
-               GemvPlan* out) {
+//  * pipelined kernel: (lanes_per_row, k_split) minimising the issue-cost
+//    model above over 32/16/8/4 lanes and splits 1..8 no larger than the
+//    chunk steps (ties go to the wider row, then the smaller split), with
+//    the row groups per pass that cover the longest row-lane range (at most
+//    4, beyond that several passes);
+//  * direct kernel: the width among 32/16/8/4 lanes that leaves the fewest
+//    idle lane slots over K/64 chunks, and the smallest split that still
+//    gives each row lane of 8/k_split warps a full pass of rows, capped by
+//    the number of chunk steps.
+bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int num_sms,
+               int ctas_per_sm, GemvPlan* out) {
   if (M < 0 || K < 0 || L < 0 || num_sms < 1 || ctas_per_sm < 1 || out == nullptr) return false;
   if (kernel < -1 || kernel > kKernelAsync) return false;
   const int64_t kchunks = K / 64;
   if (kernel == -1) kernel = kchunks > 0 ? kKernelAsync : kKernelDirect;
   if (kernel == kKernelAsync && kchunks == 0) return false;
-  int lpr = 32;
-  int64_t best_slots = -1;
-  for (int cand : {32, 16, 8, 4}) {
-    const int64_t slots = (kchunks + cand - 1) / cand * cand;
-    if (best_slots < 0 || slots < best_slots) {
-      best_slots = slots;
-      lpr = cand;
-    }
-  }
-  const int64_t steps = (kchunks + lpr - 1) / lpr;
   const int64_t rows = M * L;
-  const int64_t nr = rows_per_pass(kernel, lpr);
   int64_t ctas = (int64_t)num_sms * ctas_per_sm;
   const int64_t by_rows = (rows + kRowsPerPass - 1) / kRowsPerPass;
   if (by_rows < ctas) ctas = by_rows;
   if (ctas < 1) ctas = 1;
-  int ks = 1;
-  while (ks < kGemvWarps && 2 * ks <= steps && rows * ks < ctas * kGemvWarps * nr) ks *= 2;
+  int lpr = 32, ks = 1, groups = 1;
+  if (kernel == kKernelAsync) {
+    double best = -1.0;
+    for (int cand : {32, 16, 8, 4}) {
+      const int64_t steps = (kchunks + cand - 1) / cand;
+      for (int k = 1; k <= kGemvWarps && k <= steps; k *= 2) {
+        const int g = async_groups(M, L, permuted, cand, k, ctas);
+        const double c = async_cost(M, L, permuted, kchunks, cand, k, ctas, g);
+        if (best < 0.0 || c < best) {
+          best = c;
+          lpr = cand;
+          ks = k;
+          groups = g;
+        }
+      }
+    }
+  } else {
+    int64_t best_slots = -1;
+    for (int cand : {32, 16, 8, 4}) {
+      const int64_t slots = (kchunks + cand - 1) / cand * cand;
+      if (best_slots < 0 || slots < best_slots) {
+        best_slots = slots;
+        lpr = cand;
+      }
+    }
+    const int64_t steps = (kchunks + lpr - 1) / lpr;
+    while (ks < kGemvWarps && 2 * ks <= steps && rows * ks < ctas * kGemvWarps * kRowsPerPass)
+      ks *= 2;
+  }
   out->kernel = kernel;
   out->lanes_per_row = lpr;
   out->k_split = ks;
+  out->groups = groups;
   out->ctas = ctas;
-  out->steps = steps;
+  out->steps = (kchunks + lpr - 1) / lpr;
   return true;
 }
 
@@ -180,7 +253,8 @@ nvfp4_status_t nvfp4_gemv(const void* a, const void* b, const void* sfa, const v
   cudaError_t err = device_info(&sms, &occ, nullptr);
   if (err != cudaSuccess) return cuda_failure(err);
   GemvPlan plan;
-  if (!plan_gemv(M, K, L, -1, sms, occ, &plan)) return NVFP4_ERR_INVALID_VALUE;
+  if (!plan_gemv(M, K, L, sf_layout == NVFP4_SF_PERMUTED_128x4, -1, sms, occ, &plan))
+    return NVFP4_ERR_INVALID_VALUE;
   return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, (cudaStream_t)stream);
 }
 
@@ -207,6 +281,10 @@ nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa
   plan.k_split = k_split;
   plan.ctas = ctas;
   plan.steps = steps;
+  plan.groups = kernel == kKernelAsync
+                    ? async_groups(M, L, sf_layout == NVFP4_SF_PERMUTED_128x4, lanes_per_row,
+                                   k_split, ctas)
+                    : 1;
   return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, (cudaStream_t)stream);
 }
 
@@ -253,13 +331,13 @@ nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, i
   if (st != NVFP4_OK) return st;
   GemvPlan plan;
   if (kernel < -1 || kernel > kKernelAsync) return NVFP4_ERR_INVALID_VALUE;
-  if (!plan_gemv(M, K, L, kernel, num_sms, ctas_per_sm > 0 ? ctas_per_sm : kGemvMinCtasPerSm,
-                 &plan))
+  if (!plan_gemv(M, K, L, sf_layout == NVFP4_SF_PERMUTED_128x4, kernel, num_sms,
+                 ctas_per_sm > 0 ? ctas_per_sm : kGemvMinCtasPerSm, &plan))
     return NVFP4_ERR_UNSUPPORTED_SHAPE;
   out->kernel = plan.kernel;
   out->lanes_per_row = plan.lanes_per_row;
   out->k_split = plan.k_split;
-  out->rows_per_pass = rows_per_pass(plan.kernel, plan.lanes_per_row);
+  out->rows_per_pass = rows_per_pass(plan);
   out->threads_per_cta = kGemvThreads;
   out->ctas = plan.ctas;
   out->steps = plan.steps;

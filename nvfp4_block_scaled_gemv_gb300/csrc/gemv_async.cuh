@@ -36,91 +36,85 @@ __device__ __forceinline__ int64_t async_row(int64_t rp) {
   return (rp & ~(int64_t)127) + 32 * (t / RI) + chunk * RI + (t % RI);
 }
 
-// The (pass, K step) tasks of one warp: passes of NR = NI*RI rows of one
-// batch over the row lane's range and, in each pass, the steps ks, ks + KS,
-// ... below p.steps (the planner keeps KS <= steps, so every pass has one).
-// What a lane needs per pass (pointers to its item-0 row of A, scales and
-// c, and which items are real rows) is computed once when the pass starts;
-// item i sits a fixed kernel-wide stride further, and a task adds only its K
-// offset.
-template <int LPR, bool PERM>
+// The (K step, group) tasks of one warp.  A row lane's range is cut into
+// passes of up to G groups of NR = NI*RI rows, a pass never crossing a batch;
+// inside a pass the warp's K steps ks, ks + KS, ... (below p.steps; the
+// planner keeps KS <= steps, so every pass has one) run outermost and the
+// groups innermost, so one decoded chunk of b serves every group of the pass
+// and the partial sums are reduced and stored once per pass.  The cursor is
+// pure bookkeeping: the loader turns a task into addresses when it issues it.
+template <int LPR, int G>
 struct TaskCursor {
   static constexpr int NI = kAsyncItems, RI = 32 / LPR, NR = NI * RI;
-  static constexpr int ROW_STEP = PERM ? 32 : RI;  // rows between a lane's items
-  int64_t r, end;        // first visit-order row of the pass, end of the range
-  int64_t l_begin;       // first visit row of the pass's batch
-  int64_t l_end;         // first visit row of the next batch
-  int64_t lm;            // l * M
-  int l, cnt, s;
+  int64_t r, end;         // first visit-order row of the pass, end of the range
+  int64_t l_begin, l_end; // visit rows of the pass's batch
+  int l;                  // the pass's batch
+  int cnt;                // rows in the pass, at most G*NR
+  int ng;                 // groups in the pass, ceil(cnt / NR)
+  int s, g;               // the task: K step and group
   bool done;
-  uint32_t valid;        // bit i: the lane's item i is a real row
-  const uint8_t* a0;     // the lane's item-0 row of A
-  const uint8_t* s0;     // plain: its scale row; permuted: its 16-byte atom run (kt = 0)
-  int64_t c0;            // index of its item-0 output
 
-  __device__ __forceinline__ void start_pass(const GemvParams& p, int ks, int sub) {
+  __device__ __forceinline__ void start_pass(const GemvParams& p, int ks) {
     done = r >= end;
     if (done) return;
     if (r >= l_end) {  // passes never cross a batch, and advance by at most one
       ++l;
       l_begin = l_end;
       l_end += p.rows_per_l;
-      lm += p.M;
     }
     const int64_t left = min(end, l_end) - r;
-    cnt = left < NR ? (int)left : NR;
+    cnt = left < G * NR ? (int)left : G * NR;
+    ng = (cnt + NR - 1) / NR;
     s = ks;
-    const int64_t rp = r - l_begin;  // visit row of the pass inside its batch
-    valid = 0;
-    if (!PERM) {
-      c0 = lm + rp + sub;
-      s0 = p.sfa + c0 * p.blocks;
-#pragma unroll
-      for (int i = 0; i < NI; ++i)
-        if (i * RI + sub < cnt) valid |= 1u << i;
-    } else {
-      const int64_t m0 = async_row<true, RI>(rp + sub);  // item i is row m0 + 32*i
-      c0 = lm + m0;
-      s0 = p.sfa + (((int64_t)l * p.rest_m + (m0 >> 7)) * p.rest_k) * 512 + (m0 & 31) * 16;
-#pragma unroll
-      for (int i = 0; i < NI; ++i)
-        if (i * RI + sub < cnt && m0 + 32 * i < p.M) valid |= 1u << i;
-    }
-    a0 = p.a + c0 * p.half_k;
+    g = 0;
   }
-  __device__ __forceinline__ void init(const GemvParams& p, int64_t begin, int64_t e, int ks,
-                                       int sub) {
+  __device__ __forceinline__ void init(const GemvParams& p, int64_t begin, int64_t e, int ks) {
     r = begin;
     end = e;
-    l = (int)(begin < e ? begin / p.rows_per_l : 0);
+    l = begin < e ? batch_of(p, begin) : 0;
     l_begin = (int64_t)l * p.rows_per_l;
     l_end = l_begin + p.rows_per_l;
-    lm = (int64_t)l * p.M;
-    start_pass(p, ks, sub);
+    start_pass(p, ks);
   }
-  __device__ __forceinline__ void advance(const GemvParams& p, int ks, int KS, int sub) {
+  __device__ __forceinline__ void advance(const GemvParams& p, int ks, int KS) {
+    if (++g < ng) return;
+    g = 0;
     s += KS;
     if (s >= p.steps) {
       r += cnt;
-      start_pass(p, ks, sub);
+      start_pass(p, ks);
     }
   }
 };
 
-template <int LPR, int KS, bool PERM>
+// Which of a lane's NI items (rows first + i*RI of the pass, first = the
+// lane's offset inside the pass) are real rows.  m0 is the row of item 0;
+// permuted item i is row m0 + 32*i, and rows past M are atom padding.
+template <int LPR, bool PERM>
+__device__ __forceinline__ uint32_t item_mask(int first, int cnt, int64_t m0, int64_t M) {
+  constexpr int NI = kAsyncItems, RI = 32 / LPR;
+  uint32_t v = 0;
+#pragma unroll
+  for (int i = 0; i < NI; ++i)
+    if (first + i * RI < cnt && (!PERM || m0 + 32 * i < M)) v |= 1u << i;
+  return v;
+}
+
+template <int LPR, int KS, bool PERM, int G>
 __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
     nvfp4_gemv_async_kernel(const GemvParams p) {
-  using Cursor = TaskCursor<LPR, PERM>;
+  using Cursor = TaskCursor<LPR, G>;
   constexpr int NI = Cursor::NI;           // row items per lane per task
   constexpr int RI = Cursor::RI;           // rows per warp-wide item
-  constexpr int NR = Cursor::NR;           // rows per pass
+  constexpr int NR = Cursor::NR;           // rows per group
   constexpr int WR = kGemvWarps / KS;      // row lanes per CTA
   constexpr int S = kAsyncStages;
   constexpr int SFA_OFF = NI * 1024;       // scale words ([lane][item] words) follow the A chunks
   static_assert(LPR >= NI && LPR <= 32 && (LPR & (LPR - 1)) == 0, "LPR in {4,8,16,32}");
   static_assert(KS >= 1 && KS <= kGemvWarps && (kGemvWarps % KS) == 0, "KS divides 8");
+  static_assert(G == 1 || G == 2 || G == 4, "G in {1,2,4}");
   extern __shared__ __align__(128) uint8_t ring_smem[];
-  __shared__ float red[KS > 1 ? WR : 1][KS][NR];
+  __shared__ float red[KS > 1 ? WR : 1][KS][KS > 1 ? G * NR : 1];
 
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -140,36 +134,63 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
 
   // Plain: ranges balanced to one row.  Permuted: balanced to one aligned
   // NR-row chunk (chunks never straddle a 128-row block or a batch).
-  const int64_t unit = PERM ? NR : 1;
-  const int64_t T = p.rows_total / unit;
-  const int64_t c0 = T * (int64_t)blockIdx.x / gridDim.x;
-  const int64_t c1 = T * (int64_t)(blockIdx.x + 1) / gridDim.x;
-  const int64_t r_begin = (c0 + (c1 - c0) * wr / WR) * unit;
-  const int64_t r_end = (c0 + (c1 - c0) * (wr + 1) / WR) * unit;
+  constexpr int64_t unit = PERM ? NR : 1;
+  int64_t r_begin, r_end;
+  row_lane_units<WR>(p, wr, r_begin, r_end);
+  r_begin *= unit;
+  r_end *= unit;
 
   pdl_wait();
 
-  const int64_t a_step = (int64_t)Cursor::ROW_STEP * p.half_k;
-  const int64_t s_step = (int64_t)Cursor::ROW_STEP * p.blocks;
+  const int64_t a_step = (int64_t)(PERM ? 32 : RI) * p.half_k;  // item i -> i+1 of A
+  const int64_t s_step = (int64_t)RI * p.blocks;                // same for plain scales
+  const int64_t a_group = (int64_t)NR * p.half_k;               // plain: group g -> g+1
+  const int64_t s_group = (int64_t)NR * p.blocks;
 
-  // copy this lane's part of task t (A chunks and scale words of its rows)
-  auto issue = [&](const Cursor& t, int slot) {
+  // plain: the lane's item-0 row of A and of the scales in group 0 of the
+  // loader's current pass (recomputed when the pass changes)
+  int64_t base_r = -1;
+  const uint8_t* a_pass = p.a;
+  const uint8_t* s_pass = p.sfa;
+
+  // Copy this lane's part of task t (A chunks and scale words of its items);
+  // returns which items were copied (none when the lane's K chunk is past K).
+  auto issue = [&](const Cursor& t, int slot) -> uint32_t {
     const int kt = t.s * LPR + kc;
-    if (kt >= p.kchunks) return;
+    if (kt >= p.kchunks) return 0u;
     const uint32_t a_dst = ring + (uint32_t)(slot * kAsyncStageBytes + lane * 32);
     const uint32_t s_dst = ring + (uint32_t)(slot * kAsyncStageBytes + SFA_OFF + lane * 16);
-    const uint8_t* a_src = t.a0 + kt * 32;
+    const uint8_t* a_src;
+    const uint8_t* s_src;
+    int64_t m0 = 0;
+    if (!PERM) {
+      if (t.r != base_r) {
+        base_r = t.r;
+        const int64_t row = (int64_t)t.l * p.M + (t.r - t.l_begin) + sub;
+        a_pass = p.a + row * p.half_k;
+        s_pass = p.sfa + row * p.blocks;
+      }
+      a_src = a_pass + t.g * a_group + kt * 32;
+      s_src = s_pass + t.g * s_group + kt * 4;
+    } else {
+      m0 = async_row<true, RI>(t.r - t.l_begin + t.g * NR + sub);
+      a_src = p.a + ((int64_t)t.l * p.M + m0) * p.half_k + kt * 32;
+      // the four rows m0 + 32*i of this lane are one 16-byte run of the atom
+      // (padding rows of the last block included, read as 0x00)
+      s_src = p.sfa + (((int64_t)t.l * p.rest_m + (m0 >> 7)) * p.rest_k + kt) * 512 +
+              (m0 & 31) * 16;
+    }
+    const uint32_t valid = item_mask<LPR, PERM>(t.g * NR + sub, t.cnt, m0, p.M);
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
-      if (t.valid & (1u << i)) {
+      if (valid & (1u << i)) {
         cp_async_16(a_dst + i * 1024, a_src + i * a_step);
         cp_async_16(a_dst + i * 1024 + 16, a_src + i * a_step + 16);
-        if (!PERM) cp_async_4(s_dst + i * 4, t.s0 + kt * 4 + i * s_step);
+        if (!PERM) cp_async_4(s_dst + i * 4, s_src + i * s_step);
       }
     }
-    // permuted: the four rows m0 + 32*i of this lane are one 16-byte run of
-    // the atom (padding rows of the last block included, read as 0x00)
-    if (PERM) cp_async_16(s_dst, t.s0 + (int64_t)kt * 512);
+    if (PERM) cp_async_16(s_dst, s_src);
+    return valid;
   };
   auto load_b = [&](int l, int kt, uint32_t (&w)[8], uint32_t& sw) {
     if (kt < p.kchunks) {
@@ -180,130 +201,177 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
   };
 
   Cursor ld, cp;
-  ld.init(p, r_begin, r_end, ks, sub);
+  ld.init(p, r_begin, r_end, ks);
   cp = ld;
+  // b (and sfb) words of the next K step whose chunk differs from the one
+  // decoded (the first one requested ahead of the A stream); decoded: the
+  // lane's four blocks in its half-swapped order
+  uint32_t bw_n[8] = {0, 0, 0, 0, 0, 0, 0, 0}, sbw_n = 0;
+  bool b_pending = false;
+  if (!cp.done) {
+    load_b(cp.l, cp.s * LPR + kc, bw_n, sbw_n);
+    b_pending = true;
+  }
+  // items copied per task in flight, oldest first (the slot order)
+  uint32_t mq[S];
+#pragma unroll
+  for (int j = 0; j < S; ++j) mq[j] = 0u;
 #pragma unroll
   for (int j = 0; j < S - 1; ++j) {
     if (!ld.done) {
-      issue(ld, j);
-      ld.advance(p, ks, KS, sub);
+      mq[j] = issue(ld, j);
+      ld.advance(p, ks, KS);
     }
     cp_async_commit();
   }
-  // b (and sfb) of the task being computed, and of the next one when it differs
-  uint32_t bw[8] = {0, 0, 0, 0, 0, 0, 0, 0}, sbw = 0;
-  uint32_t bw_n[8] = {0, 0, 0, 0, 0, 0, 0, 0}, sbw_n = 0;
-  if (!cp.done) load_b(cp.l, cp.s * LPR + kc, bw, sbw);
-
-  float acc[NI];
+  uint32_t bh[4][8];
+  float sb[4];
 #pragma unroll
-  for (int i = 0; i < NI; ++i) acc[i] = 0.f;
+  for (int q = 0; q < 4; ++q) {
+    sb[q] = 0.f;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) bh[q][t] = 0;
+  }
+
+  float acc[G][NI];
+#pragma unroll
+  for (int gg = 0; gg < G; ++gg)
+#pragma unroll
+    for (int i = 0; i < NI; ++i) acc[gg][i] = 0.f;
   int slot = 0;
-  bool pending_b = false;
 
   while (!cp.done) {
-    // the slot computed in the previous iteration is free again
+    // the slot computed in the previous iteration is free again; refill it
+    // first, so the copies never queue behind a wait for b
+    mq[S - 1] = 0u;
     if (!ld.done) {
-      issue(ld, (slot + S - 1) % S);
-      ld.advance(p, ks, KS, sub);
+      mq[S - 1] = issue(ld, (slot + S - 1) % S);
+      ld.advance(p, ks, KS);
     }
     cp_async_commit();
-    // the next task's b: same K step of the next pass, or the next step;
-    // it changes unless there is one step per row and the batch stays
     const bool last_step = cp.s + KS >= p.steps;
-    const bool more = !last_step || cp.r + cp.cnt < cp.end;
-    const int s_n = last_step ? ks : cp.s + KS;
-    const int l_n = (last_step && cp.r + cp.cnt >= cp.l_end) ? cp.l + 1 : cp.l;
-    // b loaded during the previous task moves in only now, so its load
-    // latency is hidden behind a whole task's compute
-    if (pending_b) {
+    if (cp.g == 0) {
+      if (b_pending) {
+        // the chunk loaded during the previous step is decoded only now, so
+        // its load latency hides behind a whole step's compute
 #pragma unroll
-      for (int j = 0; j < 8; ++j) bw[j] = bw_n[j];
-      sbw = sbw_n;
-      pending_b = false;
-    }
-    const bool new_b = more && (s_n != cp.s || l_n != cp.l);
-    if (new_b) {
-      load_b(l_n, s_n * LPR + kc, bw_n, sbw_n);
-      pending_b = true;
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t w0 = swp ? bw_n[(2 * q + 4) & 7] : bw_n[2 * q];
+          const uint32_t w1 = swp ? bw_n[(2 * q + 5) & 7] : bw_n[2 * q + 1];
+          uint32_t d[4];
+          e2m1x8_to_f16x2x4(w0, d);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) bh[q][t] = d[t];
+          e2m1x8_to_f16x2x4(w1, d);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) bh[q][4 + t] = d[t];
+        }
+        const uint32_t sbwr = __funnelshift_l(sbw_n, sbw_n, rot16);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sb[q] = scale_of(sbwr, q);
+        b_pending = false;
+      }
+      // the next step's chunk: the same pass's next step, else the first step
+      // of the next pass (whose batch may be the next one)
+      const bool more = !last_step || cp.r + cp.cnt < cp.end;
+      const int s_n = last_step ? ks : cp.s + KS;
+      const int l_n = (last_step && cp.r + cp.cnt >= cp.l_end) ? cp.l + 1 : cp.l;
+      if (more && (s_n != cp.s || l_n != cp.l)) {
+        load_b(l_n, s_n * LPR + kc, bw_n, sbw_n);
+        b_pending = true;
+      }
     }
     cp_async_wait<S - 1>();
 
-    const int kt = cp.s * LPR + kc;
-    if (kt < p.kchunks) {
+    const uint32_t valid = mq[0];
+    // whole tasks (every lane, every item) take a branch-free path, so the
+    // items' independent dependency chains can interleave
+    const bool full = __all_sync(0xffffffffu, valid == (1u << NI) - 1u);
+    if (valid != 0u) {
       // Lanes with bit 2 set process the chunk's second 16-byte half (blocks
-      // 2, 3) first; their b words and scale bytes are rotated to match, so the
-      // block order inside registers stays static.
+      // 2, 3) first; their b blocks and scale bytes are rotated to match, so
+      // the block order inside registers stays static.
       const uint8_t* a_slot = ring_gen + slot * kAsyncStageBytes + lane * 32;
       const uint4 sw4 =
           *reinterpret_cast<const uint4*>(ring_gen + slot * kAsyncStageBytes + SFA_OFF + lane * 16);
       const uint32_t sws[4] = {sw4.x, sw4.y, sw4.z, sw4.w};
-      uint32_t bwr[8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        bwr[j] = swp ? bw[4 + j] : bw[j];
-        bwr[4 + j] = swp ? bw[j] : bw[4 + j];
-      }
-      const uint32_t sbwr = __funnelshift_l(sbw, sbw, rot16);
       uint32_t saw[NI];
 #pragma unroll
       for (int i = 0; i < NI; ++i) saw[i] = __funnelshift_l(sws[i], sws[i], rot16);
+      auto item = [&](float& a, int i, int j) {
+        const uint4 x = *reinterpret_cast<const uint4*>(a_slot + i * 1024 + ((j * 16) ^ h0));
+        const uint32_t sa2 =
+            j ? e4m3x2_half_to_f16x2<true>(saw[i]) : e4m3x2_half_to_f16x2<false>(saw[i]);
+        a = block_accumulate<false>(block_dot(x.x, x.y, bh[2 * j]), sa2, sb[2 * j], a);
+        a = block_accumulate<true>(block_dot(x.z, x.w, bh[2 * j + 1]), sa2, sb[2 * j + 1], a);
+      };
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        uint32_t bh0[8], bh1[8];
-        {
-          uint32_t q[4];
-          e2m1x8_to_f16x2x4(bwr[4 * j], q);
+      for (int gg = 0; gg < G; ++gg) {
+        if (gg != cp.g) continue;
+        if (full) {
 #pragma unroll
-          for (int t = 0; t < 4; ++t) bh0[t] = q[t];
-          e2m1x8_to_f16x2x4(bwr[4 * j + 1], q);
+          for (int j = 0; j < 2; ++j)
 #pragma unroll
-          for (int t = 0; t < 4; ++t) bh0[4 + t] = q[t];
-          e2m1x8_to_f16x2x4(bwr[4 * j + 2], q);
+            for (int i = 0; i < NI; ++i) item(acc[gg][i], i, j);
+        } else {
 #pragma unroll
-          for (int t = 0; t < 4; ++t) bh1[t] = q[t];
-          e2m1x8_to_f16x2x4(bwr[4 * j + 3], q);
+          for (int j = 0; j < 2; ++j)
 #pragma unroll
-          for (int t = 0; t < 4; ++t) bh1[4 + t] = q[t];
-        }
-        const float sb0 = scale_of(sbwr, 2 * j), sb1 = scale_of(sbwr, 2 * j + 1);
-#pragma unroll
-        for (int i = 0; i < NI; ++i) {
-          if (cp.valid & (1u << i)) {
-            const uint4 x = *reinterpret_cast<const uint4*>(a_slot + i * 1024 + ((j * 16) ^ h0));
-            const uint32_t sa2 = e4m3x2_to_f16x2(saw[i] >> (16 * j));
-            acc[i] = block_accumulate<false>(block_dot(x.x, x.y, bh0), sa2, sb0, acc[i]);
-            acc[i] = block_accumulate<true>(block_dot(x.z, x.w, bh1), sa2, sb1, acc[i]);
-          }
+            for (int i = 0; i < NI; ++i)
+              if (valid & (1u << i)) item(acc[gg][i], i, j);
         }
       }
     }
 
-    if (last_step) {
-      float v = lane_reduce<NI, LPR / 2>(acc, lane);
+    if (last_step && cp.g == cp.ng - 1) {
+      // end of the pass: every group's rows are complete in this warp
       const int rho_out = (kc / (LPR / NI)) * RI + sub;
       const bool holder = (kc % (LPR / NI)) == 0;
+      float v[G];
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg)
+        if (gg < cp.ng) v[gg] = lane_reduce<NI, LPR / 2>(acc[gg], lane);
       if constexpr (KS > 1) {
-        if (holder) red[wr][ks][rho_out] = v;
+        if (holder) {
+#pragma unroll
+          for (int gg = 0; gg < G; ++gg)
+            if (gg < cp.ng) red[wr][ks][gg * NR + rho_out] = v[gg];
+        }
         named_barrier_sync(1 + wr, 32 * KS);
         if (ks == 0 && holder) {
-          float t = red[wr][0][rho_out];
 #pragma unroll
-          for (int j = 1; j < KS; ++j) t += red[wr][j][rho_out];
-          v = t;
+          for (int gg = 0; gg < G; ++gg) {
+            if (gg < cp.ng) {
+              float t = red[wr][0][gg * NR + rho_out];
+#pragma unroll
+              for (int j = 1; j < KS; ++j) t += red[wr][j][gg * NR + rho_out];
+              v[gg] = t;
+            }
+          }
         }
         named_barrier_sync(1 + wr, 32 * KS);
       }
-      // a holder keeps item rho_out / RI of its own lane group (rho_out % RI
-      // == sub), so its cursor knows the row
-      const int item = rho_out / RI;
-      if ((KS == 1 || ks == 0) && holder && (cp.valid & (1u << item)))
-        p.c[cp.c0 + item * Cursor::ROW_STEP] = __half_as_ushort(__float2half_rn(v));
+      if ((KS == 1 || ks == 0) && holder) {
+        const int64_t rp = cp.r - cp.l_begin;
+        const int64_t lm = (int64_t)cp.l * p.M;
 #pragma unroll
-      for (int i = 0; i < NI; ++i) acc[i] = 0.f;
+        for (int gg = 0; gg < G; ++gg) {
+          if (gg < cp.ng && gg * NR + rho_out < cp.cnt) {
+            const int64_t m = PERM ? async_row<true, RI>(rp + gg * NR + rho_out)
+                                   : rp + gg * NR + rho_out;
+            if (!PERM || m < p.M) p.c[lm + m] = __half_as_ushort(__float2half_rn(v[gg]));
+          }
+        }
+      }
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg)
+#pragma unroll
+        for (int i = 0; i < NI; ++i) acc[gg][i] = 0.f;
     }
-    cp.advance(p, ks, KS, sub);
+    cp.advance(p, ks, KS);
     slot = (slot + 1 == S) ? 0 : slot + 1;
+#pragma unroll
+    for (int j = 0; j + 1 < S; ++j) mq[j] = mq[j + 1];
   }
   cp_async_wait<0>();
 }
@@ -311,15 +379,18 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
 template <bool PERM>
 cudaError_t launch_async_layout(const GemvParams& p, const GemvPlan& plan, cudaStream_t stream) {
   void (*kern)(GemvParams) = nullptr;
-#define NVFP4_CASE(LPR_, KS_) \
-  if (plan.lanes_per_row == LPR_ && plan.k_split == KS_) kern = nvfp4_gemv_async_kernel<LPR_, KS_, PERM>;
+#define NVFP4_CASE(LPR_, KS_, G_)                                             \
+  if (plan.lanes_per_row == LPR_ && plan.k_split == KS_ && plan.groups == G_) \
+    kern = nvfp4_gemv_async_kernel<LPR_, KS_, PERM, G_>;
+#define NVFP4_CASES_G(LPR_, KS_) NVFP4_CASE(LPR_, KS_, 1) NVFP4_CASE(LPR_, KS_, 2) NVFP4_CASE(LPR_, KS_, 4)
 #define NVFP4_CASES_KS(LPR_) \
-  NVFP4_CASE(LPR_, 1) NVFP4_CASE(LPR_, 2) NVFP4_CASE(LPR_, 4) NVFP4_CASE(LPR_, 8)
+  NVFP4_CASES_G(LPR_, 1) NVFP4_CASES_G(LPR_, 2) NVFP4_CASES_G(LPR_, 4) NVFP4_CASES_G(LPR_, 8)
   NVFP4_CASES_KS(4)
   NVFP4_CASES_KS(8)
   NVFP4_CASES_KS(16)
   NVFP4_CASES_KS(32)
 #undef NVFP4_CASES_KS
+#undef NVFP4_CASES_G
 #undef NVFP4_CASE
   if (kern == nullptr) return cudaErrorInvalidConfiguration;
   cudaError_t err =

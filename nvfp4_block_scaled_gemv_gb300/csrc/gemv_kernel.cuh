@@ -46,6 +46,33 @@ __device__ __forceinline__ int64_t visited_row(int64_t rp) {
   return (rp & ~(int64_t)127) + 32 * (t >> 1) + 2 * j + (t & 1);
 }
 
+// Units [begin, end) of row lane wr (of WR) in this CTA.  CTA b takes units
+// [floor(T*b/ctas), floor(T*(b+1)/ctas)) of the T = units_q*ctas + units_r
+// units (the extra units spread evenly over the grid), computed as
+// units_q*b + floor(units_r*b/ctas) with a 32-bit division whenever
+// units_r*b fits; a CTA's units are cut evenly (to one unit) among its row
+// lanes.
+__device__ __forceinline__ int64_t cta_first_unit(const GemvParams& p, uint64_t b) {
+  const uint64_t n = (uint64_t)gridDim.x;
+  const uint64_t rb = (uint64_t)p.units_r * b;
+  const uint64_t extra = rb <= 0xffffffffull ? (uint64_t)((uint32_t)rb / (uint32_t)n) : rb / n;
+  return (int64_t)((uint64_t)p.units_q * b + extra);
+}
+template <int WR>
+__device__ __forceinline__ void row_lane_units(const GemvParams& p, int wr, int64_t& begin,
+                                               int64_t& end) {
+  const int64_t c0 = cta_first_unit(p, blockIdx.x);
+  const uint64_t len = (uint64_t)(cta_first_unit(p, blockIdx.x + 1ull) - c0);
+  begin = c0 + (int64_t)(len * (uint64_t)wr / WR);
+  end = c0 + (int64_t)(len * (uint64_t)(wr + 1) / WR);
+}
+
+// Batch of visit row r (32-bit division whenever the rows fit in 32 bits).
+__device__ __forceinline__ int batch_of(const GemvParams& p, int64_t r) {
+  if (p.rows_total <= 0xffffffffll) return (int)((uint32_t)r / (uint32_t)p.rows_per_l);
+  return (int)(r / p.rows_per_l);
+}
+
 // Byte offset of the 4 scale bytes (blocks 4kt..4kt+3) of row m, chunk 0.
 template <bool PERM>
 __device__ __forceinline__ int64_t scale_row_offset(const GemvParams& p, int64_t l, int64_t m) {
@@ -130,16 +157,14 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
 
   pdl_launch_dependents();
 
-  const int64_t T = p.rows_total;
-  const int64_t c0 = T * (int64_t)blockIdx.x / gridDim.x;
-  const int64_t c1 = T * (int64_t)(blockIdx.x + 1) / gridDim.x;
-  const int64_t r_begin = c0 + (c1 - c0) * wr / WR;
-  const int64_t r_end = c0 + (c1 - c0) * (wr + 1) / WR;
+  int64_t r_begin, r_end;
+  row_lane_units<WR>(p, wr, r_begin, r_end);
 
   pdl_wait();
 
+  int64_t l = r_begin < r_end ? batch_of(p, r_begin) : 0;
   for (int64_t r = r_begin; r < r_end;) {
-    const int64_t l = r / p.rows_per_l;
+    if (r >= (l + 1) * p.rows_per_l) ++l;  // passes never cross a batch
     const int64_t batch_end = (l + 1) * p.rows_per_l;
     const int64_t pass_end = min(min(r_end, r + kRowsPerPass), batch_end);
     const int cnt = (int)(pass_end - r);

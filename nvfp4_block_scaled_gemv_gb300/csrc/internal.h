@@ -31,6 +31,8 @@ struct GemvParams {
   int64_t M;
   int64_t rows_per_l; // rows visited per batch: M (plain) or 128*rest_m (permuted)
   int64_t rows_total; // rows_per_l * L
+  int64_t units_q;    // partition of T = units_q*ctas + units_r units of rows (a unit is
+  int32_t units_r;    //   one row, or one aligned row group) evenly over the CTAs
   int32_t half_k;     // K/2: bytes of one packed row
   int32_t blocks;     // K/16: scale bytes of one plain row
   int32_t kchunks;    // K/64: 32-byte chunks per row (one per 128x4 atom column)
@@ -43,6 +45,7 @@ struct GemvPlan {
   int kernel;         // KernelKind
   int lanes_per_row;  // 4, 8, 16 or 32
   int k_split;        // 1, 2, 4 or 8 warps per row range
+  int groups;         // pipelined kernel: row groups per pass (1, 2 or 4); direct: 1
   int64_t ctas;
   int64_t steps;
 };
@@ -50,10 +53,14 @@ struct GemvPlan {
 // Host-only schedule choice (no CUDA calls) for one kernel, or for the
 // kernel the library picks (kernel = -1).  Returns false if the kernel cannot
 // run the shape (caller validates the shape first).
-bool plan_gemv(int64_t M, int64_t K, int64_t L, int kernel, int num_sms, int ctas_per_sm,
-               GemvPlan* out);
-// Rows one warp reduces at once in a kernel with a lane width.
-int rows_per_pass(int kernel, int lanes_per_row);
+bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int num_sms,
+               int ctas_per_sm, GemvPlan* out);
+// Row groups per pass of the pipelined kernel for a launch shape: enough for
+// the longest row-lane range, rounded up to 1, 2 or 4.
+int async_groups(int64_t M, int64_t L, bool permuted, int lanes_per_row, int k_split,
+                 int64_t ctas);
+// Rows one warp reduces at once under a plan.
+int rows_per_pass(const GemvPlan& plan);
 
 // Occupancy of the GEMV kernel family on the current device (CTAs per SM).
 cudaError_t gemv_ctas_per_sm(int* out);

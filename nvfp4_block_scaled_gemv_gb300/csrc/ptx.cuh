@@ -41,6 +41,22 @@ __device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) 
       : "r"(w));
 }
 
+// Two E4M3 codes (the low, or with HI the high, 16 bits of v) -> f16x2.
+// Exact; NaN stays NaN.
+template <bool HI>
+__device__ __forceinline__ uint32_t e4m3x2_half_to_f16x2(uint32_t v) {
+  uint32_t out;
+  if (HI)
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}"
+        : "=r"(out)
+        : "r"(v));
+  else
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t}"
+        : "=r"(out)
+        : "r"(v));
+  return out;
+}
+
 // Two E4M3 codes (low 16 bits of v) -> f16x2.  Exact; NaN stays NaN.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
   uint32_t out;

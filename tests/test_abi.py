@@ -116,25 +116,56 @@ BENCH_SHAPES = [(128, 256, 1), (7168, 2048, 4), (4096, 7168, 8), (7168, 16384, 1
                 (16384, 8192, 16)]
 
 
-@pytest.mark.parametrize("shape,kernel,want", [
-    (BENCH_SHAPES[0], -1, (1, 4, 1, 16, 32)),
-    (BENCH_SHAPES[1], -1, (1, 32, 1, 304, 4)),
-    (BENCH_SHAPES[2], -1, (1, 16, 1, 304, 8)),
-    (BENCH_SHAPES[3], -1, (1, 32, 2, 304, 4)),
-    (BENCH_SHAPES[4], -1, (1, 32, 1, 304, 4)),
-    (BENCH_SHAPES[0], 0, (0, 4, 1, 16, 8)),
-    (BENCH_SHAPES[1], 0, (0, 32, 1, 304, 8)),
-    (BENCH_SHAPES[2], 0, (0, 16, 1, 304, 8)),
-    (BENCH_SHAPES[3], 0, (0, 32, 4, 304, 8)),
-    (BENCH_SHAPES[4], 0, (0, 32, 1, 304, 8)),
+@pytest.mark.parametrize("shape,layout,kernel,want", [
+    (BENCH_SHAPES[0], 0, -1, (1, 32, 1, 16, 4)),
+    (BENCH_SHAPES[1], 0, -1, (1, 32, 1, 304, 16)),
+    (BENCH_SHAPES[2], 0, -1, (1, 16, 1, 304, 16)),
+    (BENCH_SHAPES[3], 0, -1, (1, 32, 4, 304, 16)),
+    (BENCH_SHAPES[4], 0, -1, (1, 8, 1, 304, 64)),
+    (BENCH_SHAPES[0], 1, -1, (1, 32, 1, 16, 4)),
+    (BENCH_SHAPES[1], 1, -1, (1, 32, 1, 304, 16)),
+    (BENCH_SHAPES[2], 1, -1, (1, 16, 1, 304, 16)),
+    (BENCH_SHAPES[3], 1, -1, (1, 32, 4, 304, 16)),
+    (BENCH_SHAPES[4], 1, -1, (1, 32, 1, 304, 16)),
+    (BENCH_SHAPES[0], 0, 0, (0, 4, 1, 16, 8)),
+    (BENCH_SHAPES[1], 0, 0, (0, 32, 1, 304, 8)),
+    (BENCH_SHAPES[2], 0, 0, (0, 16, 1, 304, 8)),
+    (BENCH_SHAPES[3], 0, 0, (0, 32, 4, 304, 8)),
+    (BENCH_SHAPES[4], 0, 0, (0, 32, 1, 304, 8)),
 ])
-def test_plan_for_the_benchmark_shapes(lib, shape, kernel, want):
+def test_plan_for_the_benchmark_shapes(lib, shape, layout, kernel, want):
     M, K, L = shape
-    plan = nv.nvfp4_gemv_plan(M, K, L, nv.SF_PLAIN, num_sms=152, ctas_per_sm=2, kernel=kernel)
+    plan = nv.nvfp4_gemv_plan(M, K, L, layout, num_sms=152, ctas_per_sm=2, kernel=kernel)
     got = tuple(plan[k] for k in ("kernel", "lanes_per_row", "k_split", "ctas", "rows_per_pass"))
     assert got == want
     assert plan["steps"] == -(-(K // 64) // plan["lanes_per_row"])
-    assert plan == nv.nvfp4_gemv_plan(M, K, L, nv.SF_PERMUTED_128x4, 152, 2, kernel=kernel)
+
+
+def max_rows_per_row_lane(M, L, perm, lpr, ks, ctas):
+    """Longest row-lane range of the pipelined kernel's partition."""
+    nr = 4 * (32 // lpr)
+    unit = nr if perm else 1
+    rows_per_l = -(-M // 128) * 128 if perm else M
+    t = rows_per_l * L // unit
+    per_cta = -(-t // ctas)
+    return -(-per_cta // (8 // ks)) * unit
+
+
+def test_pipelined_rows_per_pass_cover_the_longest_range(lib):
+    """rows_per_pass = groups * 4 * (32 / lanes_per_row), with the fewest of
+    1, 2 or 4 groups that hold the longest row-lane range."""
+    rng = np.random.default_rng(1)
+    for _ in range(300):
+        M, L = int(rng.integers(1, 30000)), int(rng.integers(1, 17))
+        K = 64 * int(rng.integers(1, 300))
+        layout = int(rng.integers(0, 2))
+        plan = nv.nvfp4_gemv_plan(M, K, L, layout, 152, 2)
+        nr = 4 * (32 // plan["lanes_per_row"])
+        rows = max_rows_per_row_lane(M, L, layout == 1, plan["lanes_per_row"], plan["k_split"],
+                                     plan["ctas"])
+        need = -(-rows // nr)
+        groups = 1 if need <= 1 else 2 if need <= 2 else 4
+        assert plan["rows_per_pass"] == groups * nr
 
 
 def test_kernel_choice(lib):
@@ -174,6 +205,14 @@ def visited_row(rp, perm):
     return (rp & ~127) + 32 * (t >> 1) + 2 * j + (t & 1)
 
 
+def cta_units(T, ctas, cta):
+    """Units [c0, c1) of one CTA: floor(T*b/ctas), as q*b + floor(r*b/ctas)."""
+    q, r = divmod(T, ctas)
+    first = lambda b: q * b + (r * b) // ctas
+    assert first(cta) == T * cta // ctas
+    return first(cta), first(cta + 1)
+
+
 def partition(M, L, ctas, ks, perm, nr=8):
     """Rows each (cta, row lane, pass of nr rows) handles, as (l, m) pairs."""
     rows_per_l = ((M + 127) // 128) * 128 if perm else M
@@ -181,7 +220,7 @@ def partition(M, L, ctas, ks, perm, nr=8):
     wr_count = 8 // ks
     seen = []
     for cta in range(ctas):
-        c0, c1 = T * cta // ctas, T * (cta + 1) // ctas
+        c0, c1 = cta_units(T, ctas, cta)
         for wr in range(wr_count):
             r, r_end = c0 + (c1 - c0) * wr // wr_count, c0 + (c1 - c0) * (wr + 1) // wr_count
             while r < r_end:
@@ -238,26 +277,40 @@ def test_pipelined_permuted_order_shares_scale_runs(ri):
                 assert offs == [offs[0] + 4 * g for g in range(4)] and offs[0] % 16 == 0
 
 
+@pytest.mark.parametrize("groups", [1, 2, 4])
+@pytest.mark.parametrize("perm", [False, True])
 @pytest.mark.parametrize("M,L,ctas,ks,ri", [(1, 1, 1, 1, 1), (129, 2, 37, 2, 2), (7168, 4, 304, 1, 1),
-                                            (1000, 3, 13, 4, 8), (200, 1, 600, 8, 4)])
-def test_pipelined_permuted_chunks_cover_every_row_once(M, L, ctas, ks, ri):
+                                            (1000, 3, 13, 4, 8), (200, 1, 600, 8, 4),
+                                            (333, 5, 7, 1, 2)])
+def test_pipelined_tasks_cover_every_row_once(M, L, ctas, ks, ri, perm, groups):
+    """Model of the pipelined kernel's work split: row-lane ranges, passes of
+    up to groups*nr rows inside one batch, and in each group the items
+    i*ri + sub of every lane group sub."""
     nr = 4 * ri
-    rows_per_l = ((M + 127) // 128) * 128
-    T = rows_per_l * L // nr
+    unit = nr if perm else 1
+    rows_per_l = ((M + 127) // 128) * 128 if perm else M
+    T = rows_per_l * L // unit
     wr_count = 8 // ks
     seen = []
     for cta in range(ctas):
-        c0, c1 = T * cta // ctas, T * (cta + 1) // ctas
+        c0, c1 = cta_units(T, ctas, cta)
         for wr in range(wr_count):
-            r = (c0 + (c1 - c0) * wr // wr_count) * nr
-            r_end = (c0 + (c1 - c0) * (wr + 1) // wr_count) * nr
+            r = (c0 + (c1 - c0) * wr // wr_count) * unit
+            r_end = (c0 + (c1 - c0) * (wr + 1) // wr_count) * unit
             while r < r_end:
                 l = r // rows_per_l
-                cnt = min(r_end, r + nr, (l + 1) * rows_per_l) - r
-                assert cnt == nr  # aligned chunks: every pass is one whole chunk
-                for rho in range(cnt):
-                    m = async_row(r - l * rows_per_l + rho, True, ri)
-                    if m < M:
-                        seen.append((l, m))
+                cnt = min(r_end, r + groups * nr, (l + 1) * rows_per_l) - r
+                if perm:
+                    assert cnt % nr == 0  # aligned chunks: whole groups only
+                ng = -(-cnt // nr)
+                for g in range(ng):
+                    for sub in range(ri):
+                        m0 = async_row(r - l * rows_per_l + g * nr + sub, perm, ri)
+                        for i in range(4):
+                            if g * nr + i * ri + sub >= cnt:
+                                continue
+                            m = m0 + (32 * i if perm else i * ri)
+                            if m < M:
+                                seen.append((l, m))
                 r += cnt
     assert sorted(seen) == [(l, m) for l in range(L) for m in range(M)]

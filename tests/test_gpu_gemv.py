@@ -103,7 +103,9 @@ def test_every_schedule(kernel, lpr, ks):
     p = synthetic.make_problem(M, K, L, seed=lpr * 10 + ks)
     ref, sums, sumabs = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
     outs = []
-    for ctas in (1, 7, 64, 600):
+    # grid sizes that give the pipelined kernel 1, 2 and 4 row groups per pass
+    # and several passes per row lane
+    for ctas in (1, 5, 13, 40, 150, 600):
         for layout in (nv.SF_PLAIN, nv.SF_PERMUTED_128x4):
             got = run(p, M, K, L, layout, schedule=(kernel, lpr, ks, ctas))
             parity.assert_parity(got, ref, sums, sumabs,
