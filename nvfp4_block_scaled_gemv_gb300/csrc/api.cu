@@ -142,22 +142,24 @@ int64_t max_rows_per_row_lane(int64_t M, int64_t L, bool permuted, int lanes_per
   return (per_cta + lanes - 1) / lanes * unit;
 }
 
-// Rough issue cost of the busiest warp under a pipelined schedule, in warp
-// instructions: item chunks (decode, dot, scale), tasks (copies, loop),
-// decoded b chunks, and per pass the lane reduction and store of each group
-// plus the K-split exchange.
+// Relative cost of a pipelined schedule for the busiest row lane: every
+// task (one K step of one row group) pays its loop, copy and item-mask work,
+// every distinct chunk of b is loaded and decoded once, and every row group
+// pays its share of the pass-end lane reduction and store.  The weights
+// were fitted to measured schedule sweeps on GB300 over the benchmark
+// shapes and several other decode-sized shapes (M 512..28672, K 1024..16384,
+// L 1..16, both scale layouts); the item arithmetic itself is the same for
+// every schedule and does not enter.
 double async_cost(int64_t M, int64_t L, bool permuted, int64_t kchunks, int lpr, int ks,
                   int64_t ctas, int groups) {
-  const int64_t ri = 32 / lpr, nr = kAsyncItems * ri;
+  const int64_t nr = kAsyncItems * (32 / lpr);
   const int64_t steps = (kchunks + lpr - 1) / lpr;
   const int64_t steps_w = (steps + ks - 1) / ks;
   const int64_t rows = max_rows_per_row_lane(M, L, permuted, lpr, ks, ctas);
   const int64_t ngroups = (rows + nr - 1) / nr;
   const int64_t passes = (ngroups + groups - 1) / groups;
-  const int64_t items = (rows + ri - 1) / ri;
   const int64_t b_chunks = steps_w > 1 ? passes * steps_w : 1;
-  return 85.0 * items * steps_w + 45.0 * ngroups * steps_w + 45.0 * b_chunks +
-         passes * (50.0 + (ks > 1 ? 80.0 : 0.0)) + 25.0 * ngroups;
+  return 49.0 * ngroups * steps_w + 109.0 * b_chunks + 161.0 * ngroups;
 }
 
 }  // namespace
@@ -176,11 +178,11 @@ int async_groups(int64_t M, int64_t L, bool permuted, int lanes_per_row, int k_s
 //    kernel writes the zeros of K == 0;
 //  * ctas: one wave of resident CTAs (SMs x occupancy), fewer for tiny
 //    problems (at least 8 rows per CTA);
-//  * pipelined kernel: (lanes_per_row, k_split) minimising the issue-cost
-//    model above over 32/16/8/4 lanes and splits 1..8 no larger than the
-//    chunk steps (ties go to the wider row, then the smaller split), with
-//    the row groups per pass that cover the longest row-lane range (at most
-//    4, beyond that several passes);
+//  * pipelined kernel: (lanes_per_row, k_split) minimising the cost model
+//    above over 32/16/8/4 lanes (16/8/4 for permuted scales) and splits
+//    1..8 no larger than the chunk steps (ties go to the wider row, then the
+//    smaller split), with the row groups per pass that cover the longest
+//    row-lane range (at most 4, beyond that several passes);
 //  * direct kernel: the width among 32/16/8/4 lanes that leaves the fewest
 //    idle lane slots over K/64 chunks, and the smallest split that still
 //    gives each row lane of 8/k_split warps a full pass of rows, capped by
@@ -201,6 +203,9 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
   if (kernel == kKernelAsync) {
     double best = -1.0;
     for (int cand : {32, 16, 8, 4}) {
+      // a lane's permuted scale run is 16 bytes: with 32 lanes per row it is
+      // half of a 32-byte sector whose other half another task reads
+      if (permuted && cand == 32) continue;
       const int64_t steps = (kchunks + cand - 1) / cand;
       for (int k = 1; k <= kGemvWarps && k <= steps; k *= 2) {
         const int g = async_groups(M, L, permuted, cand, k, ctas);

@@ -118,15 +118,15 @@ BENCH_SHAPES = [(128, 256, 1), (7168, 2048, 4), (4096, 7168, 8), (7168, 16384, 1
 
 @pytest.mark.parametrize("shape,layout,kernel,want", [
     (BENCH_SHAPES[0], 0, -1, (1, 32, 1, 16, 4)),
-    (BENCH_SHAPES[1], 0, -1, (1, 32, 1, 304, 16)),
+    (BENCH_SHAPES[1], 0, -1, (1, 16, 1, 304, 16)),
     (BENCH_SHAPES[2], 0, -1, (1, 16, 1, 304, 16)),
     (BENCH_SHAPES[3], 0, -1, (1, 32, 4, 304, 16)),
     (BENCH_SHAPES[4], 0, -1, (1, 8, 1, 304, 64)),
-    (BENCH_SHAPES[0], 1, -1, (1, 32, 1, 16, 4)),
-    (BENCH_SHAPES[1], 1, -1, (1, 32, 1, 304, 16)),
+    (BENCH_SHAPES[0], 1, -1, (1, 16, 1, 16, 8)),
+    (BENCH_SHAPES[1], 1, -1, (1, 16, 1, 304, 16)),
     (BENCH_SHAPES[2], 1, -1, (1, 16, 1, 304, 16)),
-    (BENCH_SHAPES[3], 1, -1, (1, 32, 4, 304, 16)),
-    (BENCH_SHAPES[4], 1, -1, (1, 32, 1, 304, 16)),
+    (BENCH_SHAPES[3], 1, -1, (1, 16, 8, 304, 32)),
+    (BENCH_SHAPES[4], 1, -1, (1, 8, 1, 304, 64)),
     (BENCH_SHAPES[0], 0, 0, (0, 4, 1, 16, 8)),
     (BENCH_SHAPES[1], 0, 0, (0, 32, 1, 304, 8)),
     (BENCH_SHAPES[2], 0, 0, (0, 16, 1, 304, 8)),
@@ -166,6 +166,14 @@ def test_pipelined_rows_per_pass_cover_the_longest_range(lib):
         need = -(-rows // nr)
         groups = 1 if need <= 1 else 2 if need <= 2 else 4
         assert plan["rows_per_pass"] == groups * nr
+
+
+def test_permuted_plans_avoid_half_sector_scale_reads(lib):
+    rng = np.random.default_rng(2)
+    for _ in range(200):
+        M, L = int(rng.integers(1, 30000)), int(rng.integers(1, 17))
+        K = 64 * int(rng.integers(1, 300))
+        assert nv.nvfp4_gemv_plan(M, K, L, nv.SF_PERMUTED_128x4, 152, 2)["lanes_per_row"] != 32
 
 
 def test_kernel_choice(lib):
