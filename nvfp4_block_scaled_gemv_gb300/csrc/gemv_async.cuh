@@ -1,22 +1,26 @@
 // NVFP4 block-scaled batched GEMV, per-warp cp.async pipelined kernel (sm_103a).
 //
-// Same work split and arithmetic as the direct kernel (gemv_kernel.cuh): CTA
-// row ranges balanced to one row, row lanes of KS warps, LPR lanes per row,
+// Same arithmetic as the direct kernel (gemv_kernel.cuh): LPR lanes per row,
 // 32-byte K chunks per lane, exact half2 block dots, fp32 block scaling, a
 // shuffle butterfly over the lanes of a row and a fixed-order shared-memory
-// sum over the K-split warps.  What changes is how A reaches the registers:
+// sum over the KS warps that split a row's K range.  What differs is how A
+// reaches the registers and how a warp orders its work:
 //
-//   * A warp's work is a sequence of tasks, one task = one K step of one pass
-//     (kAsyncItems row items per lane).  Each lane copies its own A chunks and
-//     scale words of a task into a per-warp ring of kAsyncStages shared-memory
-//     slots with cp.async, and waits for them with its own wait_group: a lane
-//     only ever reads bytes it copied, so no cross-lane synchronisation is
-//     needed and no register holds in-flight data.
-//   * The warp keeps kAsyncStages - 1 tasks in flight while it computes one,
-//     so every warp streams continuously instead of alternating between a
-//     burst of loads and a burst of arithmetic.
-//   * The lane's 32 bytes of b (and its sfb word) are loaded into registers
-//     one task ahead.
+//   * A row lane's rows are cut into passes of up to G groups of NR rows,
+//     never crossing a batch.  A pass runs the warp's K steps outermost and
+//     its groups innermost; one task = one group at one K step (kAsyncItems
+//     row items per lane).  The lane's chunk of b is decoded once per K step
+//     and serves every group, and the partial sums are reduced and stored
+//     once per pass.
+//   * Each lane copies its own A chunks and scale words of a task into a
+//     per-warp ring of kAsyncStages shared-memory slots with cp.async and
+//     waits for them with its own wait_group: a lane only ever reads bytes it
+//     copied, so there is no cross-lane synchronisation and no spin-wait.
+//   * The warp keeps kAsyncStages - 1 tasks in flight while it computes one.
+//     The loader runs that far ahead of the compute and hands it, per task,
+//     the mask of items it copied.
+//   * The next K step's b words are loaded while the current step computes
+//     and decoded when that step begins.
 #pragma once
 #include "gemv_kernel.cuh"
 
