@@ -142,24 +142,30 @@ int64_t max_rows_per_row_lane(int64_t M, int64_t L, bool permuted, int lanes_per
   return (per_cta + lanes - 1) / lanes * unit;
 }
 
-// Relative cost of a pipelined schedule for the busiest row lane: every
-// task (one K step of one row group) pays its loop, copy and item-mask work,
-// every distinct chunk of b is loaded and decoded once, and every row group
-// pays its share of the pass-end lane reduction and store.  The weights
-// were fitted to measured schedule sweeps on GB300 over the benchmark
-// shapes and several other decode-sized shapes (M 512..28672, K 1024..16384,
-// L 1..16, both scale layouts); the item arithmetic itself is the same for
-// every schedule and does not enter.
+// Relative cost of a pipelined schedule.  Dominant term: the average number
+// of tasks per warp (one task = one row group at one K step), which charges
+// the lanes left idle when K/64 is not a multiple of the row width.  Then:
+// passes of more than 4 K steps per warp, charged for sweeping their rows'
+// columns over a long window (DRAM locality); the busiest row lane's decoded
+// b chunks and row groups (pass-end work).  The weights were fitted to
+// measured sweeps of all 16 schedules on GB300 over the benchmark shapes and
+// several other decode-sized shapes (M 512..28672, K 1024..16384, L 1..16,
+// both scale layouts); ties go to the wider row, then the smaller split.
 double async_cost(int64_t M, int64_t L, bool permuted, int64_t kchunks, int lpr, int ks,
-                  int64_t ctas, int groups) {
+                  int64_t ctas) {
   const int64_t nr = kAsyncItems * (32 / lpr);
   const int64_t steps = (kchunks + lpr - 1) / lpr;
   const int64_t steps_w = (steps + ks - 1) / ks;
+  const int64_t rows_per_l = permuted ? (M + 127) / 128 * 128 : M;
+  const double avg_rows = (double)(rows_per_l * L) / (double)(ctas * (kGemvWarps / ks));
+  const double avg_tasks = avg_rows / (double)nr * (double)steps_w;
   const int64_t rows = max_rows_per_row_lane(M, L, permuted, lpr, ks, ctas);
   const int64_t ngroups = (rows + nr - 1) / nr;
-  const int64_t passes = (ngroups + groups - 1) / groups;
+  const int64_t g = ngroups <= 1 ? 1 : ngroups <= 2 ? 2 : ngroups <= 4 ? 4 : 2;
+  const int64_t passes = (ngroups + g - 1) / g;
   const int64_t b_chunks = steps_w > 1 ? passes * steps_w : 1;
-  return 49.0 * ngroups * steps_w + 109.0 * b_chunks + 161.0 * ngroups;
+  const double long_pass = (double)(ngroups * steps_w * (steps_w > 4 ? steps_w - 4 : 0));
+  return 1000.0 * avg_tasks + 4.8 * (double)b_chunks + 5.6 * (double)ngroups + 32.8 * long_pass;
 }
 
 }  // namespace
@@ -169,7 +175,9 @@ int async_groups(int64_t M, int64_t L, bool permuted, int lanes_per_row, int k_s
   const int64_t nr = kAsyncItems * (32 / lanes_per_row);
   const int64_t rows = max_rows_per_row_lane(M, L, permuted, lanes_per_row, k_split, ctas);
   const int64_t g = (rows + nr - 1) / nr;
-  return g <= 1 ? 1 : g <= 2 ? 2 : 4;
+  // a range of more than 4 groups takes several passes anyway; there the
+  // 2-group kernel (fewer live accumulators) is as fast or faster
+  return g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 2;
 }
 
 // The schedule (see gemv_kernel.cuh and gemv_async.cuh for what each knob
@@ -199,7 +207,7 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
   const int64_t by_rows = (rows + kRowsPerPass - 1) / kRowsPerPass;
   if (by_rows < ctas) ctas = by_rows;
   if (ctas < 1) ctas = 1;
-  int lpr = 32, ks = 1, groups = 1;
+  int lpr = 32, ks = 1;
   if (kernel == kKernelAsync) {
     double best = -1.0;
     for (int cand : {32, 16, 8, 4}) {
@@ -208,13 +216,11 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
       if (permuted && cand == 32) continue;
       const int64_t steps = (kchunks + cand - 1) / cand;
       for (int k = 1; k <= kGemvWarps && k <= steps; k *= 2) {
-        const int g = async_groups(M, L, permuted, cand, k, ctas);
-        const double c = async_cost(M, L, permuted, kchunks, cand, k, ctas, g);
-        if (best < 0.0 || c < best) {
+        const double c = async_cost(M, L, permuted, kchunks, cand, k, ctas);
+        if (best < 0.0 || c < best - 1e-9) {
           best = c;
           lpr = cand;
           ks = k;
-          groups = g;
         }
       }
     }
@@ -234,7 +240,7 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
   out->kernel = kernel;
   out->lanes_per_row = lpr;
   out->k_split = ks;
-  out->groups = groups;
+  out->groups = kernel == kKernelAsync ? async_groups(M, L, permuted, lpr, ks, ctas) : 1;
   out->ctas = ctas;
   out->steps = (kchunks + lpr - 1) / lpr;
   return true;

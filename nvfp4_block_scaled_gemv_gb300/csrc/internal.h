@@ -56,7 +56,8 @@ struct GemvPlan {
 bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int num_sms,
                int ctas_per_sm, GemvPlan* out);
 // Row groups per pass of the pipelined kernel for a launch shape: enough for
-// the longest row-lane range, rounded up to 1, 2 or 4.
+// the longest row-lane range, rounded up to 1, 2 or 4; 2 (several passes)
+// when the range needs more than 4.
 int async_groups(int64_t M, int64_t L, bool permuted, int lanes_per_row, int k_split,
                  int64_t ctas);
 // Rows one warp reduces at once under a plan.
