@@ -102,6 +102,12 @@ GemvParams make_params(const void* a, const void* b, const void* sfa, const void
   const int64_t units = p.rows_total / unit;
   p.units_q = units / plan.ctas;
   p.units_r = (int32_t)(units % plan.ctas);
+  // L2 prefetch ahead of the dependency wait: one task per warp when the call
+  // gives each warp fewer than 4 tasks (4 KB of A each) on average, else two
+  // (measured on GB300: more prefetch delays the first copies of small calls)
+  const int64_t four_tasks = plan.ctas * kGemvWarps * 4 * (int64_t)kAsyncItems * 32 * 32;
+  const int64_t half_k = K / 2;
+  p.prefetch_tasks = (half_k > 0 && M * L >= (four_tasks + half_k - 1) / half_k) ? 2 : 1;
   return p;
 }
 

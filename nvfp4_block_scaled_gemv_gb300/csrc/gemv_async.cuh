@@ -144,8 +144,6 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
   r_begin *= unit;
   r_end *= unit;
 
-  pdl_wait();
-
   const int64_t a_step = (int64_t)(PERM ? 32 : RI) * p.half_k;  // item i -> i+1 of A
   const int64_t s_step = (int64_t)RI * p.blocks;                // same for plain scales
   const int64_t a_group = (int64_t)NR * p.half_k;               // plain: group g -> g+1
@@ -196,6 +194,26 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
     if (PERM) cp_async_16(s_dst, s_src);
     return valid;
   };
+  // Ask the L2 for the A lines of task t (used before the dependency wait:
+  // the L2 is coherent, so the copies issued after the wait still read what
+  // earlier work on the stream wrote; the prefetch only starts the DRAM
+  // traffic while that work finishes).
+  auto prefetch_task = [&](const Cursor& t) {
+    const int kt = t.s * LPR + kc;
+    if (kt >= p.kchunks) return;
+    int64_t m0 = 0, row;
+    if (!PERM) {
+      row = (int64_t)t.l * p.M + (t.r - t.l_begin) + t.g * NR + sub;
+    } else {
+      m0 = async_row<true, RI>(t.r - t.l_begin + t.g * NR + sub);
+      row = (int64_t)t.l * p.M + m0;
+    }
+    const uint8_t* a_src = p.a + row * p.half_k + kt * 32;
+    const uint32_t valid = item_mask<LPR, PERM>(t.g * NR + sub, t.cnt, m0, p.M);
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+      if (valid & (1u << i)) prefetch_l2(a_src + i * a_step);
+  };
   auto load_b = [&](int l, int kt, uint32_t (&w)[8], uint32_t& sw) {
     if (kt < p.kchunks) {
       ld_shared_256(p.b + (int64_t)l * p.half_k + kt * 32, w);
@@ -207,6 +225,14 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
   Cursor ld, cp;
   ld.init(p, r_begin, r_end, ks);
   cp = ld;
+  {
+    Cursor pf = ld;
+    for (int j = 0; j < S - 1 && j < p.prefetch_tasks && !pf.done; ++j) {
+      prefetch_task(pf);
+      pf.advance(p, ks, KS);
+    }
+  }
+  pdl_wait();
   // b (and sfb) words of the next K step whose chunk differs from the one
   // decoded (the first one requested ahead of the A stream); decoded: the
   // lane's four blocks in its half-swapped order

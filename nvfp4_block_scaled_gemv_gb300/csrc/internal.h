@@ -33,6 +33,7 @@ struct GemvParams {
   int64_t rows_total; // rows_per_l * L
   int64_t units_q;    // partition of T = units_q*ctas + units_r units of rows (a unit is
   int32_t units_r;    //   one row, or one aligned row group) evenly over the CTAs
+  int32_t prefetch_tasks;  // pipelined kernel: tasks per warp prefetched into L2 (1 or 2)
   int32_t half_k;     // K/2: bytes of one packed row
   int32_t blocks;     // K/16: scale bytes of one plain row
   int32_t kchunks;    // K/64: 32-byte chunks per row (one per 128x4 atom column)

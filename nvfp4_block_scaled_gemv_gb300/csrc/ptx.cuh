@@ -131,6 +131,11 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Hint: bring the line holding p into L2 (no data returned, no ordering).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Programmatic dependent launch: block until the preceding grid on the
 // stream has completed and its writes are visible (a no-op when the launch
 // carries no programmatic dependency).
