@@ -214,7 +214,20 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
   if (by_rows < ctas) ctas = by_rows;
   if (ctas < 1) ctas = 1;
   int lpr = 32, ks = 1;
-  if (kernel == kKernelAsync) {
+  // permuted scales with plenty of rows: 4 lanes per row, whose 32-row
+  // groups read whole 128-byte lines of the scale atoms, and the even K split
+  // that leaves about 2 K steps per warp (measured: 4-16% faster than the
+  // model's choice on the large permuted shapes, slower when rows are scarce)
+  const int64_t steps4 = (kchunks + 3) / 4;
+  int ks4 = 1;
+  while (ks4 < kGemvWarps && (steps4 + ks4 - 1) / ks4 > 2) ks4 *= 2;
+  const bool narrow = kernel == kKernelAsync && permuted && steps4 % ks4 == 0 &&
+                      steps4 / ks4 <= 4 &&
+                      (M + 127) / 128 * 128 * L >= 24 * ctas * (kGemvWarps / ks4);
+  if (narrow) {
+    lpr = 4;
+    ks = ks4;
+  } else if (kernel == kKernelAsync) {
     double best = -1.0;
     for (int cand : {32, 16, 8, 4}) {
       // a lane's permuted scale run is 16 bytes: with 32 lanes per row it is

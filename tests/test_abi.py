@@ -123,10 +123,10 @@ BENCH_SHAPES = [(128, 256, 1), (7168, 2048, 4), (4096, 7168, 8), (7168, 16384, 1
     (BENCH_SHAPES[3], 0, -1, (1, 32, 4, 304, 16)),
     (BENCH_SHAPES[4], 0, -1, (1, 32, 1, 304, 8)),
     (BENCH_SHAPES[0], 1, -1, (1, 4, 1, 16, 32)),
-    (BENCH_SHAPES[1], 1, -1, (1, 16, 1, 304, 16)),
+    (BENCH_SHAPES[1], 1, -1, (1, 4, 4, 304, 64)),
     (BENCH_SHAPES[2], 1, -1, (1, 16, 1, 304, 16)),
     (BENCH_SHAPES[3], 1, -1, (1, 16, 8, 304, 32)),
-    (BENCH_SHAPES[4], 1, -1, (1, 16, 2, 304, 16)),
+    (BENCH_SHAPES[4], 1, -1, (1, 4, 8, 304, 64)),
     (BENCH_SHAPES[0], 0, 0, (0, 4, 1, 16, 8)),
     (BENCH_SHAPES[1], 0, 0, (0, 32, 1, 304, 8)),
     (BENCH_SHAPES[2], 0, 0, (0, 16, 1, 304, 8)),
@@ -175,6 +175,17 @@ def test_permuted_plans_avoid_half_sector_scale_reads(lib):
         M, L = int(rng.integers(1, 30000)), int(rng.integers(1, 17))
         K = 64 * int(rng.integers(1, 300))
         assert nv.nvfp4_gemv_plan(M, K, L, nv.SF_PERMUTED_128x4, 152, 2)["lanes_per_row"] != 32
+
+
+def test_permuted_plans_with_plenty_of_rows_use_narrow_rows(lib):
+    """Permuted scales, at least 24 rows per row lane and an even K split to at
+    most 4 steps per warp: 4 lanes per row."""
+    assert nv.nvfp4_gemv_plan(7168, 2048, 4, nv.SF_PERMUTED_128x4, 152, 2)["lanes_per_row"] == 4
+    assert nv.nvfp4_gemv_plan(28672, 4096, 1, nv.SF_PERMUTED_128x4, 152, 2)["k_split"] == 8
+    # scarce rows: the cost model decides
+    assert nv.nvfp4_gemv_plan(2048, 4096, 1, nv.SF_PERMUTED_128x4, 152, 2)["lanes_per_row"] != 4
+    # uneven K split (28 steps over 8 warps): the cost model decides
+    assert nv.nvfp4_gemv_plan(4096, 7168, 8, nv.SF_PERMUTED_128x4, 152, 2)["lanes_per_row"] != 4
 
 
 def test_kernel_choice(lib):
