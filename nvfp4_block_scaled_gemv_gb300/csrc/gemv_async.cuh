@@ -149,6 +149,7 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
   const int64_t a_group = (int64_t)NR * p.half_k;               // plain: group g -> g+1
   const int64_t s_group = (int64_t)NR * p.blocks;
 
+  const uint64_t a_pol = l2_evict_first_policy();
   // plain: the lane's item-0 row of A and of the scales in group 0 of the
   // loader's current pass (recomputed when the pass changes)
   int64_t base_r = -1;
@@ -186,8 +187,8 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
       if (valid & (1u << i)) {
-        cp_async_16(a_dst + i * 1024, a_src + i * a_step);
-        cp_async_16(a_dst + i * 1024 + 16, a_src + i * a_step + 16);
+        cp_async_16_ef(a_dst + i * 1024, a_src + i * a_step, a_pol);
+        cp_async_16_ef(a_dst + i * 1024 + 16, a_src + i * a_step + 16, a_pol);
         if (!PERM) cp_async_4(s_dst + i * 4, s_src + i * s_step);
       }
     }
