@@ -83,8 +83,13 @@ typedef enum {
  * Alignment: a, b, sfa, sfb 32-byte aligned; c 2-byte aligned.
  * Accuracy: each 16-element block's dot product is exact; blocks are scaled
  * and summed in FP32; c is rounded to nearest even (overflow gives +-Inf;
- * a NaN scale gives NaN).  Results are bitwise reproducible run to run, and
- * identical for the two scale layouts.
+ * a NaN scale gives NaN).  Results are bitwise reproducible run to run.  The
+ * FP32 summation order follows the launch schedule, which the library picks
+ * per shape and scale layout; under one schedule (nvfp4_gemv_explicit) the
+ * two layouts give identical bits.
+ * Execution detail: before waiting for the preceding work on the stream, the
+ * kernel may ask the L2 to prefetch lines of a (a hint that returns no data;
+ * every input is read only after that work has completed).
  */
 nvfp4_status_t nvfp4_gemv(const void* a, const void* b, const void* sfa, const void* sfb,
                           void* c, int64_t M, int64_t K, int64_t L, int sf_layout,

@@ -238,3 +238,19 @@ def test_graph_capture_and_replay():
     g.replay()
     torch.cuda.synchronize()
     assert np.array_equal(bits(c), want)
+
+
+def test_random_shapes_default_schedule():
+    """Random shapes through the library's own plans (row groups per pass,
+    ragged batches, narrow permuted rows, K splits) against the oracle."""
+    rng = np.random.default_rng(2024)
+    for case in range(24):
+        M = int(rng.integers(1, 3000))
+        K = 64 * int(rng.integers(1, 129))
+        L = int(rng.integers(1, 6))
+        layout = int(rng.integers(0, 2))
+        p = synthetic.make_problem(M, K, L, seed=1000 + case)
+        ref, sums, sumabs = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
+        got = run(p, M, K, L, layout)
+        plan = nv.nvfp4_gemv_plan(M, K, L, layout, torch.cuda.get_device_properties(0).multi_processor_count, 0)
+        parity.assert_parity(got, ref, sums, sumabs, f"case {case}: M={M} K={K} L={L} layout={layout} plan={plan}")
