@@ -222,6 +222,29 @@ class DeviceProblem:
                       self.layout, stream_handle)
 
 
+class ExtProblem(DeviceProblem):
+    """DeviceProblem called through nvfp4_gemv_ex: an output scale, an fp16
+    [L][M] bias, and b as row 0 of an [L][pad_rows][K/2] buffer."""
+
+    def __init__(self, torch, nv, p, M, K, L, layout, dev, sets, pad_rows=8, alpha=0.5):
+        super().__init__(torch, nv, p, M, K, L, layout, dev, sets)
+        self.alpha = alpha
+        self.b_stride = pad_rows * (K // 2)
+        gen = torch.Generator().manual_seed(0)
+        for s in self.sets:
+            padded = torch.zeros((L, pad_rows, K // 2), dtype=torch.uint8, device=dev)
+            padded[:, 0, :] = s["b"].view(L, K // 2)
+            s["b"] = padded
+            s["bias"] = (torch.randn((L, M), generator=gen) * 4).to(torch.float16).to(dev)
+
+    def call(self, nv, i, stream_handle):
+        s = self.sets[i % len(self.sets)]
+        nv.nvfp4_gemv_ex(s["a"].data_ptr(), s["b"].data_ptr(), s["sfa"].data_ptr(),
+                         s["sfb"].data_ptr(), s["c"].data_ptr(), self.M, self.K, self.L,
+                         self.layout, alpha=self.alpha, bias=s["bias"].data_ptr(),
+                         b_batch_stride=self.b_stride, stream=stream_handle)
+
+
 def time_graph(torch, nv, prob, steps, warmup, stream):
     """Per-call microseconds over `steps` calls replayed from a CUDA graph."""
     handle = stream.cuda_stream
@@ -453,6 +476,21 @@ def run_native(args):
                                   "single_call_l2_flushed_us": round(smed, 3)}), flush=True)
                 del wprob
                 torch.cuda.empty_cache()
+        # the extended entry point on the headline shape
+        wname, wM, wK, wL = WORKLOAD
+        wp = synthetic.make_problem(wM, wK, wL, seed=0)
+        wbytes = synthetic.algorithmic_bytes(wM, wK, wL) + 2 * wL * wM  # + the bias
+        wprob = ExtProblem(torch, nv, wp, wM, wK, wL, nv.SF_PLAIN, dev, ROTATE_SETS)
+        wsteps = max(64, min(20000, int(2e9 / wbytes)) // 64 * 64)
+        wus, _, _ = time_graph(torch, nv, wprob, wsteps, 64, stream)
+        gbs = wbytes / (wus * 1e-6) / 1e9
+        print(json.dumps({"workload": wname, "scale_layout": "plain",
+                          "path": "nvfp4_gemv_ex: alpha 0.5, fp16 bias, b in an [L][8][K/2] buffer",
+                          "us_per_call": round(wus, 3), "gb_per_s": round(gbs, 1),
+                          "pct_of_hbm_peak": round(100 * gbs / peaks["hbm_gbs"], 2),
+                          "rotating_sets": ROTATE_SETS, "calls": wsteps}), flush=True)
+        del wprob
+        torch.cuda.empty_cache()
 
 
 def run_profile_case(args):

@@ -95,6 +95,43 @@ nvfp4_status_t nvfp4_gemv(const void* a, const void* b, const void* sfa, const v
                           void* c, int64_t M, int64_t K, int64_t L, int sf_layout,
                           struct CUstream_st* stream);
 
+/*
+ * Options of nvfp4_gemv_ex.  Zero-initialised fields other than alpha give
+ * the plain call; {1.0f, NULL, 0, 0} is exactly nvfp4_gemv.
+ *
+ *   alpha            : fp32 output scale: c = fp16(alpha * sum + bias).  A
+ *                      global per-tensor scale of this kind is mentioned in a
+ *                      removed docstring line of submission 69575; the pages
+ *                      never apply one (alpha = 1).
+ *   bias             : NULL, or fp16 [L][M] (row stride M) added after the
+ *                      scaling; 2-byte aligned.  With a bias the scaling and the
+ *                      addition are one fp32 fused multiply-add before the fp16
+ *                      rounding.
+ *   b_batch_stride   : bytes from batch l to batch l+1 of b; 0 = K/2 (dense).
+ *                      Otherwise >= K/2 and a multiple of 32: b may be row 0 of
+ *                      an N-padded [L][N][K/2] buffer such as the one
+ *                      submission 103289's host code builds (stride N*K/2).
+ *   sfb_batch_stride : bytes from batch l to batch l+1 of sfb; 0 = dense
+ *                      (K/16 plain, (K/64)*512 permuted).  Otherwise at least
+ *                      that, and a multiple of 4 (plain) or 16 (permuted).
+ * Violations: a stride below the dense size -> NVFP4_ERR_INVALID_VALUE; a
+ * stride or bias pointer off its alignment -> NVFP4_ERR_MISALIGNED.
+ */
+typedef struct {
+  float alpha;
+  const void* bias;
+  int64_t b_batch_stride;
+  int64_t sfb_batch_stride;
+} nvfp4_gemv_options_t;
+
+/*
+ * nvfp4_gemv with options (NULL options = nvfp4_gemv).  Same arguments,
+ * rules, schedule and accuracy contract; the tolerance scales with |alpha|.
+ */
+nvfp4_status_t nvfp4_gemv_ex(const void* a, const void* b, const void* sfa, const void* sfb,
+                             void* c, int64_t M, int64_t K, int64_t L, int sf_layout,
+                             const nvfp4_gemv_options_t* options, struct CUstream_st* stream);
+
 /* The two GEMV kernels (same arithmetic, different data movement). */
 typedef enum {
   /* Warps load up to 8 rows' 32-byte K chunks straight into registers with

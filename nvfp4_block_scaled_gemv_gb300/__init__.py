@@ -30,6 +30,7 @@ ERR_CUDA = 4
 # Every symbol include/nvfp4_gemv.h declares.
 EXPORTS = (
     "nvfp4_gemv",
+    "nvfp4_gemv_ex",
     "nvfp4_gemv_explicit",
     "nvfp4_repack_scales",
     "nvfp4_permuted_scale_bytes",
@@ -61,6 +62,11 @@ class _Plan(ctypes.Structure):
                 ("ctas", ctypes.c_int64), ("steps", ctypes.c_int64)]
 
 
+class _Options(ctypes.Structure):
+    _fields_ = [("alpha", ctypes.c_float), ("bias", ctypes.c_void_p),
+                ("b_batch_stride", ctypes.c_int64), ("sfb_batch_stride", ctypes.c_int64)]
+
+
 _lib = None
 
 
@@ -77,6 +83,8 @@ def library() -> ctypes.CDLL:
     lib.nvfp4_gemv.argtypes = [P, P, P, P, P, I64, I64, I64, I, P]
     lib.nvfp4_gemv.restype = I
     lib.nvfp4_gemv_explicit.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, I, I, I64, P]
+    lib.nvfp4_gemv_ex.restype = I
+    lib.nvfp4_gemv_ex.argtypes = [P, P, P, P, P, I64, I64, I64, I, ctypes.POINTER(_Options), P]
     lib.nvfp4_gemv_explicit.restype = I
     lib.nvfp4_repack_scales.argtypes = [P, P, I64, I64, I64, P]
     lib.nvfp4_repack_scales.restype = I
@@ -105,6 +113,16 @@ def nvfp4_gemv(a: int, b: int, sfa: int, sfb: int, c: int, M: int, K: int, L: in
                sf_layout: int = SF_PLAIN, stream: int = 0) -> None:
     """Enqueue c = GEMV(a, b, sfa, sfb) on ``stream`` (device pointers as ints)."""
     _check(library().nvfp4_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, stream), "nvfp4_gemv")
+
+
+def nvfp4_gemv_ex(a: int, b: int, sfa: int, sfb: int, c: int, M: int, K: int, L: int,
+                  sf_layout: int = SF_PLAIN, alpha: float = 1.0, bias: int = 0,
+                  b_batch_stride: int = 0, sfb_batch_stride: int = 0, stream: int = 0) -> None:
+    """nvfp4_gemv with an output scale, an fp16 [L][M] bias (pointer or 0) and
+    batch strides for b and sfb (0 = dense)."""
+    opt = _Options(alpha, bias or None, b_batch_stride, sfb_batch_stride)
+    _check(library().nvfp4_gemv_ex(a, b, sfa, sfb, c, M, K, L, sf_layout, ctypes.byref(opt),
+                                   stream), "nvfp4_gemv_ex")
 
 
 def nvfp4_gemv_explicit(a: int, b: int, sfa: int, sfb: int, c: int, M: int, K: int, L: int,

@@ -78,8 +78,26 @@ nvfp4_status_t validate_gemv_pointers(const void* a, const void* b, const void* 
   return NVFP4_OK;
 }
 
+// The options of a plain nvfp4_gemv call: no output scale or bias, dense b
+// and sfb (strides 0 = dense).
+const nvfp4_gemv_options_t kDefaultOptions = {1.0f, nullptr, 0, 0};
+
+// Option checks shared by the entry points that take options.
+nvfp4_status_t validate_options(const nvfp4_gemv_options_t& o, int64_t K, int sf_layout) {
+  if (o.b_batch_stride < 0 || o.sfb_batch_stride < 0) return NVFP4_ERR_INVALID_VALUE;
+  if (o.b_batch_stride != 0 && o.b_batch_stride < K / 2) return NVFP4_ERR_INVALID_VALUE;
+  if (o.b_batch_stride % 32 != 0) return NVFP4_ERR_MISALIGNED;
+  const bool permuted = sf_layout == NVFP4_SF_PERMUTED_128x4;
+  const int64_t sfb_dense = permuted ? (K / 64) * 512 : K / 16;
+  if (o.sfb_batch_stride != 0 && o.sfb_batch_stride < sfb_dense) return NVFP4_ERR_INVALID_VALUE;
+  if (o.sfb_batch_stride % (permuted ? 16 : 4) != 0) return NVFP4_ERR_MISALIGNED;
+  if (o.bias != nullptr && !aligned(o.bias, 2)) return NVFP4_ERR_MISALIGNED;
+  return NVFP4_OK;
+}
+
 GemvParams make_params(const void* a, const void* b, const void* sfa, const void* sfb, void* c,
-                       int64_t M, int64_t K, int64_t L, bool permuted, const GemvPlan& plan) {
+                       int64_t M, int64_t K, int64_t L, bool permuted, const GemvPlan& plan,
+                       const nvfp4_gemv_options_t& opt) {
   GemvParams p;
   p.a = static_cast<const uint8_t*>(a);
   p.b = static_cast<const uint8_t*>(b);
@@ -108,14 +126,19 @@ GemvParams make_params(const void* a, const void* b, const void* sfa, const void
   const int64_t four_tasks = plan.ctas * kGemvWarps * 4 * (int64_t)kAsyncItems * 32 * 32;
   const int64_t half_k = K / 2;
   p.prefetch_tasks = (half_k > 0 && M * L >= (four_tasks + half_k - 1) / half_k) ? 2 : 1;
+  p.b_stride = opt.b_batch_stride != 0 ? opt.b_batch_stride : K / 2;
+  p.sfb_stride = opt.sfb_batch_stride != 0 ? opt.sfb_batch_stride
+                                           : (permuted ? (int64_t)p.rest_k * 512 : K / 16);
+  p.alpha = opt.alpha;
+  p.bias = static_cast<const uint16_t*>(opt.bias);
   return p;
 }
 
 nvfp4_status_t run_gemv(const void* a, const void* b, const void* sfa, const void* sfb, void* c,
                         int64_t M, int64_t K, int64_t L, int sf_layout, const GemvPlan& plan,
-                        cudaStream_t stream) {
+                        const nvfp4_gemv_options_t& opt, cudaStream_t stream) {
   const bool permuted = sf_layout == NVFP4_SF_PERMUTED_128x4;
-  const GemvParams p = make_params(a, b, sfa, sfb, c, M, K, L, permuted, plan);
+  const GemvParams p = make_params(a, b, sfa, sfb, c, M, K, L, permuted, plan, opt);
   cudaError_t err;
   if (plan.kernel == kKernelAsync)
     err = permuted ? launch_async_permuted(p, plan, stream) : launch_async_plain(p, plan, stream);
@@ -274,7 +297,16 @@ extern "C" {
 nvfp4_status_t nvfp4_gemv(const void* a, const void* b, const void* sfa, const void* sfb,
                           void* c, int64_t M, int64_t K, int64_t L, int sf_layout,
                           struct CUstream_st* stream) {
+  return nvfp4_gemv_ex(a, b, sfa, sfb, c, M, K, L, sf_layout, nullptr, stream);
+}
+
+nvfp4_status_t nvfp4_gemv_ex(const void* a, const void* b, const void* sfa, const void* sfb,
+                             void* c, int64_t M, int64_t K, int64_t L, int sf_layout,
+                             const nvfp4_gemv_options_t* options, struct CUstream_st* stream) {
   nvfp4_status_t st = validate_gemv_shape(M, K, L, sf_layout);
+  if (st != NVFP4_OK) return st;
+  const nvfp4_gemv_options_t& opt = options ? *options : kDefaultOptions;
+  st = validate_options(opt, K, sf_layout);
   if (st != NVFP4_OK) return st;
   if (M == 0 || L == 0) return NVFP4_OK;
   st = validate_gemv_pointers(a, b, sfa, sfb, c, K);
@@ -285,7 +317,7 @@ nvfp4_status_t nvfp4_gemv(const void* a, const void* b, const void* sfa, const v
   GemvPlan plan;
   if (!plan_gemv(M, K, L, sf_layout == NVFP4_SF_PERMUTED_128x4, -1, sms, occ, &plan))
     return NVFP4_ERR_INVALID_VALUE;
-  return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, (cudaStream_t)stream);
+  return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, opt, (cudaStream_t)stream);
 }
 
 nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa,
@@ -315,7 +347,8 @@ nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa
                     ? async_groups(M, L, sf_layout == NVFP4_SF_PERMUTED_128x4, lanes_per_row,
                                    k_split, ctas)
                     : 1;
-  return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, (cudaStream_t)stream);
+  return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, kDefaultOptions,
+                  (cudaStream_t)stream);
 }
 
 nvfp4_status_t nvfp4_repack_scales(const void* src, void* dst, int64_t rows, int64_t K,

@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
   constexpr int S = kAsyncStages;
   constexpr int SFA_OFF = NI * 1024;       // scale words ([lane][item] words) follow the A chunks
   static_assert(LPR >= NI && LPR <= 32 && (LPR & (LPR - 1)) == 0, "LPR in {4,8,16,32}");
-  static_assert(KS >= 1 && KS <= kGemvWarps && (kGemvWarps % KS) == 0, "KS divides 8");
+  static_assert(KS >= 1 && KS <= kGemvWarps && (kGemvWarps % KS) == 0, "KS divides the warps per CTA");
   static_assert(G == 1 || G == 2 || G == 4, "G in {1,2,4}");
   extern __shared__ __align__(128) uint8_t ring_smem[];
   __shared__ float red[KS > 1 ? WR : 1][KS][KS > 1 ? G * NR : 1];
@@ -217,9 +217,8 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
   };
   auto load_b = [&](int l, int kt, uint32_t (&w)[8], uint32_t& sw) {
     if (kt < p.kchunks) {
-      ld_shared_256(p.b + (int64_t)l * p.half_k + kt * 32, w);
-      sw = ld_scale_32(p.sfb + (PERM ? ((int64_t)l * p.rest_k + kt) * 512
-                                     : (int64_t)l * p.blocks + kt * 4));
+      ld_shared_256(p.b + (int64_t)l * p.b_stride + kt * 32, w);
+      sw = ld_scale_32(p.sfb + (int64_t)l * p.sfb_stride + (PERM ? (int64_t)kt * 512 : kt * 4));
     }
   };
 
@@ -390,7 +389,7 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
           if (gg < cp.ng && gg * NR + rho_out < cp.cnt) {
             const int64_t m = PERM ? async_row<true, RI>(rp + gg * NR + rho_out)
                                    : rp + gg * NR + rho_out;
-            if (!PERM || m < p.M) p.c[lm + m] = __half_as_ushort(__float2half_rn(v[gg]));
+            if (!PERM || m < p.M) p.c[lm + m] = finish_output(p, v[gg], lm + m);
           }
         }
       }

@@ -73,6 +73,15 @@ __device__ __forceinline__ int batch_of(const GemvParams& p, int64_t r) {
   return (int)(r / p.rows_per_l);
 }
 
+// c[idx] from the row's fp32 sum v: fp16(alpha * v + bias[idx]) rounded to
+// nearest even, with one fp32 rounding before it (a fused multiply-add when
+// there is a bias; alpha = 1 without one gives v itself).
+__device__ __forceinline__ uint16_t finish_output(const GemvParams& p, float v, int64_t idx) {
+  const float o = p.bias ? fmaf(v, p.alpha, __half2float(__ushort_as_half(p.bias[idx])))
+                         : v * p.alpha;
+  return __half_as_ushort(__float2half_rn(o));
+}
+
 // Byte offset of the 4 scale bytes (blocks 4kt..4kt+3) of row m, chunk 0.
 template <bool PERM>
 __device__ __forceinline__ int64_t scale_row_offset(const GemvParams& p, int64_t l, int64_t m) {
@@ -147,7 +156,7 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
   constexpr int NI = kRowsPerPass / RI;   // loads per lane per chunk step
   constexpr int WR = kGemvWarps / KS;     // row lanes per CTA
   static_assert(LPR >= 4 && LPR <= 32 && (LPR & (LPR - 1)) == 0, "LPR in {4,8,16,32}");
-  static_assert(KS >= 1 && KS <= kGemvWarps && (kGemvWarps % KS) == 0, "KS divides 8");
+  static_assert(KS >= 1 && KS <= kGemvWarps && (kGemvWarps % KS) == 0, "KS divides the warps per CTA");
   __shared__ float red[KS > 1 ? WR : 1][KS][kRowsPerPass];
 
   const int lane = threadIdx.x & 31;
@@ -180,8 +189,8 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
       a_off[i] = (l * p.M + m) * p.half_k;
       s_off[i] = scale_row_offset<PERM>(p, l, m);
     }
-    const uint8_t* brow = p.b + l * p.half_k;
-    const uint8_t* sbrow = p.sfb + (PERM ? l * p.rest_k * 512 : l * p.blocks);
+    const uint8_t* brow = p.b + l * p.b_stride;
+    const uint8_t* sbrow = p.sfb + l * p.sfb_stride;
 
     float acc[NI];
 #pragma unroll
@@ -245,7 +254,7 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
     }
     if ((KS == 1 || ks == 0) && holder && rho_out < cnt) {
       const int64_t m = visited_row<PERM>(rp0 + rho_out);
-      if (m < p.M) p.c[l * p.M + m] = __half_as_ushort(__float2half_rn(v));
+      if (m < p.M) p.c[l * p.M + m] = finish_output(p, v, l * p.M + m);
     }
     r = pass_end;
   }

@@ -34,6 +34,10 @@ struct GemvParams {
   int64_t units_q;    // partition of T = units_q*ctas + units_r units of rows (a unit is
   int32_t units_r;    //   one row, or one aligned row group) evenly over the CTAs
   int32_t prefetch_tasks;  // pipelined kernel: tasks per warp prefetched into L2 (1 or 2)
+  int64_t b_stride;   // bytes from batch l to l+1 of b
+  int64_t sfb_stride; // bytes from batch l to l+1 of sfb
+  float alpha;        // output scale (1 = none)
+  const uint16_t* bias;  // fp16 [L][M] added after scaling, or null
   int32_t half_k;     // K/2: bytes of one packed row
   int32_t blocks;     // K/16: scale bytes of one plain row
   int32_t kchunks;    // K/64: 32-byte chunks per row (one per 128x4 atom column)

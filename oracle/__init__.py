@@ -133,6 +133,22 @@ def gemv(a, b, sfa, sfb, M: int, K: int, L: int):
     return c, s, sabs
 
 
+def gemv_ex(a, b, sfa, sfb, M: int, K: int, L: int, alpha: float = 1.0, bias=None):
+    """fp64 path with an output scale and bias: ``fp16(alpha * sum + bias)``.
+
+    ``bias`` is fp16 bits [L, M] (uint16) or None.  ``alpha * sum + bias`` is
+    formed in fp64 from the fp64 sums of :func:`gemv` and rounded to binary16
+    once.  Returns ``(c_bits, values, |alpha| * sumabs)``: the fp64 values
+    before rounding and the |term| sums scaled like the sums (the tolerance).
+    """
+    _, s, sabs = gemv(a, b, sfa, sfb, M, K, L)
+    y = np.float64(alpha) * s
+    if bias is not None:
+        bv = np.ascontiguousarray(np.asarray(bias, dtype=np.uint16)).view(np.float16)
+        y = y + bv.astype(np.float64).reshape(L, M)
+    return fp16_rne(y), y, abs(float(alpha)) * sabs
+
+
 def gemv_at(a, b, sfa, sfb, M: int, K: int, L: int, m_idx, l_idx):
     """fp64 path for the selected outputs ``(m_idx[i], l_idx[i])`` only."""
     _check_shape(M, K, L)

@@ -188,6 +188,30 @@ def test_permuted_plans_with_plenty_of_rows_use_narrow_rows(lib):
     assert nv.nvfp4_gemv_plan(4096, 7168, 8, nv.SF_PERMUTED_128x4, 152, 2)["lanes_per_row"] != 4
 
 
+def test_gemv_ex_option_validation(lib):
+    """Option errors come back before any launch (no GPU needed)."""
+    base = dict(a=64, b=64, sfa=64, sfb=64, c=64, M=8, K=2048, L=2)
+
+    def status(layout=nv.SF_PLAIN, **kw):
+        try:
+            nv.nvfp4_gemv_ex(*base.values(), layout, **kw)
+        except nv.Nvfp4Error as e:
+            return e.status
+        return nv.OK
+
+    assert status(b_batch_stride=-32) == nv.ERR_INVALID_VALUE
+    assert status(b_batch_stride=512) == nv.ERR_INVALID_VALUE           # below K/2
+    assert status(b_batch_stride=1024 + 16) == nv.ERR_MISALIGNED         # not a multiple of 32
+    assert status(sfb_batch_stride=64) == nv.ERR_INVALID_VALUE          # below K/16
+    assert status(sfb_batch_stride=130) == nv.ERR_MISALIGNED
+    assert status(nv.SF_PERMUTED_128x4, sfb_batch_stride=512) == nv.ERR_INVALID_VALUE  # below 32*512
+    assert status(nv.SF_PERMUTED_128x4, sfb_batch_stride=32 * 512 + 4) == nv.ERR_MISALIGNED
+    assert status(bias=3) == nv.ERR_MISALIGNED
+    # valid options on an empty problem: nothing to do
+    nv.nvfp4_gemv_ex(0, 0, 0, 0, 0, 0, 2048, 2, 0, alpha=2.0, b_batch_stride=4096,
+                     sfb_batch_stride=256)
+
+
 def test_kernel_choice(lib):
     assert nv.nvfp4_gemv_plan(100, 0, 3, 0, 152, 2)["kernel"] == nv.KERNEL_DIRECT
     assert nv.nvfp4_gemv_plan(100, 64, 3, 0, 152, 2)["kernel"] == nv.KERNEL_PIPELINED

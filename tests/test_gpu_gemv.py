@@ -254,3 +254,59 @@ def test_random_shapes_default_schedule():
         got = run(p, M, K, L, layout)
         plan = nv.nvfp4_gemv_plan(M, K, L, layout, torch.cuda.get_device_properties(0).multi_processor_count, 0)
         parity.assert_parity(got, ref, sums, sumabs, f"case {case}: M={M} K={K} L={L} layout={layout} plan={plan}")
+
+
+# --- nvfp4_gemv_ex: output scale, bias, batch strides of b and sfb -----------
+
+def _ex_call(a, b, sfa, sfb, c, M, K, L, layout, **kw):
+    nv.nvfp4_gemv_ex(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(), c.data_ptr(),
+                     M, K, L, layout, stream=torch.cuda.current_stream().cuda_stream, **kw)
+    torch.cuda.synchronize()
+    return bits(c).reshape(L, M)
+
+
+@pytest.mark.parametrize("layout", [nv.SF_PLAIN, nv.SF_PERMUTED_128x4])
+def test_gemv_ex_defaults_are_nvfp4_gemv(layout):
+    M, K, L = 700, 2048, 3
+    p = synthetic.make_problem(M, K, L, seed=41)
+    base = run(p, M, K, L, layout)
+    a, b, sfa, sfb = device_problem(p, M, K, L, layout)
+    c = torch.empty(L * M, dtype=torch.float16, device=DEV)
+    assert np.array_equal(_ex_call(a, b, sfa, sfb, c, M, K, L, layout), base)
+
+
+@pytest.mark.parametrize("layout", [nv.SF_PLAIN, nv.SF_PERMUTED_128x4])
+@pytest.mark.parametrize("M,K,L,alpha", [(700, 2048, 3, 0.375), (129, 7168, 2, -1.5e-3),
+                                         (4096, 1024, 2, 37.0)])
+def test_gemv_ex_alpha_bias_and_padded_b(layout, M, K, L, alpha):
+    """b as row 0 of an [L][8][K/2] buffer and sfb in a padded per-batch
+    stride, the other rows random: only row 0 may reach c."""
+    p = synthetic.make_problem(M, K, L, seed=M + K)
+    rng = np.random.default_rng(M)
+    bias = (rng.standard_normal((L, M)) * 8).astype(np.float16).view(np.uint16)
+    ref, vals, sumabs = oracle.gemv_ex(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L,
+                                       alpha=alpha, bias=bias)
+    a, b, sfa, sfb = device_problem(p, M, K, L, layout)
+    N = 8
+    b_pad = torch.from_numpy(rng.integers(0, 256, (L, N, K // 2), dtype=np.uint8)).to(DEV)
+    b_pad[:, 0, :] = b.view(L, K // 2)
+    sfb_dense = sfb.numel() // L
+    sfb_pad = torch.from_numpy(rng.integers(0, 256, (L, 2 * sfb_dense), dtype=np.uint8)).to(DEV)
+    sfb_pad[:, :sfb_dense] = sfb.view(L, sfb_dense)
+    c = torch.full((L * M,), SENTINEL, dtype=torch.float16, device=DEV)
+    bias_d = torch.from_numpy(bias.reshape(-1).copy()).to(DEV)
+    got = _ex_call(a, b_pad, sfa, sfb_pad, c, M, K, L, layout, alpha=alpha,
+                   bias=bias_d.data_ptr(), b_batch_stride=N * (K // 2),
+                   sfb_batch_stride=2 * sfb_dense)
+    parity.assert_parity(got, ref, vals, sumabs, f"ex M={M} K={K} L={L} alpha={alpha} layout={layout}")
+
+
+def test_gemv_ex_zero_k_gives_the_bias():
+    M, L = 37, 2
+    bias = (np.arange(L * M, dtype=np.float32) - 20).astype(np.float16)
+    bias_d = torch.from_numpy(bias).to(DEV)
+    c = torch.full((L * M,), SENTINEL, dtype=torch.float16, device=DEV)
+    nv.nvfp4_gemv_ex(0, 0, 0, 0, c.data_ptr(), M, 0, L, nv.SF_PLAIN, alpha=3.0,
+                     bias=bias_d.data_ptr(), stream=torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert np.array_equal(c.cpu().numpy().astype(np.float64), bias.astype(np.float64))

@@ -219,3 +219,79 @@ def test_empty_and_zero_k():
     c, _, _ = oracle.gemv(np.zeros(0, np.uint8), np.zeros(64, np.uint8), np.zeros(0, np.uint8),
                           np.zeros(8, np.uint8), 0, 128, 1)
     assert c.shape == (1, 0)
+
+
+# --- output scale and bias (nvfp4_gemv_ex) -----------------------------------
+
+def fraction_to_fp16_bits(q: Fraction) -> int:
+    """binary16 bits of an exact rational, round to nearest even (IEEE 754:
+    5 exponent bits, bias 15, 10 mantissa bits, subnormals, overflow to inf)."""
+    sign = 0x8000 if q < 0 else 0
+    q = abs(q)
+    if q == 0:
+        return sign
+    # e = floor(log2 q), no smaller than the subnormal exponent -14
+    e = q.numerator.bit_length() - q.denominator.bit_length()
+    if Fraction(2) ** e > q:
+        e -= 1
+    e = max(e, -14)
+    ulp = Fraction(2) ** (e - 10)
+    n_floor = q // ulp
+    rem = q - n_floor * ulp
+    n = n_floor + (1 if rem * 2 > ulp or (rem * 2 == ulp and n_floor % 2 == 1) else 0)
+    if n == 2048:  # rounded up to the next binade
+        n, e = 1024, e + 1
+    if e > 15:
+        return sign | 0x7C00
+    if n < 1024:  # subnormal (e == -14)
+        return sign | int(n)
+    return sign | ((e + 15) << 10) | int(n - 1024)
+
+
+def test_fraction_rounding_helper_matches_numpy_on_doubles():
+    rng = np.random.default_rng(5)
+    xs = np.concatenate([rng.standard_normal(2000) * 10.0 ** rng.integers(-9, 6, 2000),
+                         [65504.0, 65519.99, 65520.0, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26]])
+    for x in xs:
+        want = int(np.array([x]).astype(np.float16).view(np.uint16)[0])
+        assert fraction_to_fp16_bits(Fraction(float(x))) == want, x
+
+
+def test_gemv_ex_defaults_equal_gemv():
+    M, K, L = 24, 384, 3
+    p = synthetic.make_problem(M, K, L, seed=21)
+    c, s, sa = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
+    ce, y, sae = oracle.gemv_ex(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
+    assert np.array_equal(ce, c) and np.array_equal(y, s) and np.array_equal(sae, sa)
+
+
+@pytest.mark.parametrize("alpha,shift", [(2.0, 8), (0.5, -8)])
+def test_gemv_ex_power_of_two_alpha_equals_scale_exponent_change(alpha, shift):
+    """alpha = 2**e scales like moving every sfb exponent by e (codes +-8)."""
+    M, K, L = 32, 512, 2
+    p = synthetic.make_problem(M, K, L, seed=22)
+    ce, _, _ = oracle.gemv_ex(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L, alpha=alpha)
+    c2, _, _ = oracle.gemv(p["a"], p["b"], p["sfa"], (p["sfb"].astype(np.int32) + shift).astype(np.uint8),
+                           M, K, L)
+    assert np.array_equal(ce, c2)
+
+
+def test_gemv_ex_brute_force_with_alpha_and_bias():
+    rng = np.random.default_rng(23)
+    for case, alpha in enumerate([0.375, -1.25, 5.0, np.float32(0.3), np.float32(-7.1e-3)]):
+        M, K, L = int(rng.integers(1, 7)), 64 * int(rng.integers(1, 3)), int(rng.integers(1, 3))
+        p = synthetic.make_problem(M, K, L, seed=300 + case)
+        bias = (rng.standard_normal((L, M)) * 4).astype(np.float16).view(np.uint16)
+        ce, _, _ = oracle.gemv_ex(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L,
+                                  alpha=float(alpha), bias=bias)
+        for l in range(L):
+            for m in range(M):
+                total = Fraction(0)
+                for k in range(K):
+                    abyte, bbyte = int(p["a"][l, m, k // 2]), int(p["b"][l, k // 2])
+                    acode = (abyte >> 4) if k % 2 else (abyte & 15)
+                    bcode = (bbyte >> 4) if k % 2 else (bbyte & 15)
+                    total += (_e2m1_fraction(acode) * _e4m3_fraction(int(p["sfa"][l, m, k // 16]))
+                              * _e2m1_fraction(bcode) * _e4m3_fraction(int(p["sfb"][l, k // 16])))
+                y = Fraction(float(alpha)) * total + Fraction(_half_value(int(bias[l, m])))
+                assert int(ce[l, m]) == fraction_to_fp16_bits(y), (case, l, m)
