@@ -214,7 +214,8 @@ int async_groups(int64_t M, int64_t L, bool permuted, int lanes_per_row, int k_s
 //  * kernel: the pipelined (cp.async) kernel for every K > 0; the direct
 //    kernel writes the zeros of K == 0;
 //  * ctas: one wave of resident CTAs (SMs x occupancy), fewer for tiny
-//    problems (at least 8 rows per CTA);
+//    problems (at least 2 rows per CTA: short, long-K problems still spread
+//    their K splits over many SMs);
 //  * pipelined kernel: (lanes_per_row, k_split) minimising the cost model
 //    above over 32/16/8/4 lanes (16/8/4 for permuted scales) and splits
 //    1..8 no larger than the chunk steps (ties go to the wider row, then the
@@ -233,7 +234,7 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
   if (kernel == kKernelAsync && kchunks == 0) return false;
   const int64_t rows = M * L;
   int64_t ctas = (int64_t)num_sms * ctas_per_sm;
-  const int64_t by_rows = (rows + kRowsPerPass - 1) / kRowsPerPass;
+  const int64_t by_rows = (rows + 1) / 2;
   if (by_rows < ctas) ctas = by_rows;
   if (ctas < 1) ctas = 1;
   int lpr = 32, ks = 1;

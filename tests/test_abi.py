@@ -117,17 +117,17 @@ BENCH_SHAPES = [(128, 256, 1), (7168, 2048, 4), (4096, 7168, 8), (7168, 16384, 1
 
 
 @pytest.mark.parametrize("shape,layout,kernel,want", [
-    (BENCH_SHAPES[0], 0, -1, (1, 4, 1, 16, 32)),
+    (BENCH_SHAPES[0], 0, -1, (1, 4, 1, 64, 32)),
     (BENCH_SHAPES[1], 0, -1, (1, 16, 1, 304, 16)),
     (BENCH_SHAPES[2], 0, -1, (1, 16, 1, 304, 16)),
     (BENCH_SHAPES[3], 0, -1, (1, 32, 4, 304, 16)),
     (BENCH_SHAPES[4], 0, -1, (1, 32, 1, 304, 8)),
-    (BENCH_SHAPES[0], 1, -1, (1, 4, 1, 16, 32)),
+    (BENCH_SHAPES[0], 1, -1, (1, 4, 1, 64, 32)),
     (BENCH_SHAPES[1], 1, -1, (1, 4, 4, 304, 64)),
     (BENCH_SHAPES[2], 1, -1, (1, 16, 1, 304, 16)),
     (BENCH_SHAPES[3], 1, -1, (1, 16, 8, 304, 32)),
     (BENCH_SHAPES[4], 1, -1, (1, 4, 8, 304, 64)),
-    (BENCH_SHAPES[0], 0, 0, (0, 4, 1, 16, 8)),
+    (BENCH_SHAPES[0], 0, 0, (0, 4, 1, 64, 8)),
     (BENCH_SHAPES[1], 0, 0, (0, 32, 1, 304, 8)),
     (BENCH_SHAPES[2], 0, 0, (0, 16, 1, 304, 8)),
     (BENCH_SHAPES[3], 0, 0, (0, 32, 4, 304, 8)),
