@@ -310,3 +310,15 @@ def test_gemv_ex_zero_k_gives_the_bias():
                      bias=bias_d.data_ptr(), stream=torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert np.array_equal(c.cpu().numpy().astype(np.float64), bias.astype(np.float64))
+
+
+@pytest.mark.parametrize("layout", [nv.SF_PLAIN, nv.SF_PERMUTED_128x4])
+@pytest.mark.parametrize("M,K,L", [(1, 64, 1000), (100000, 64, 1), (3, 16384, 7), (129, 128, 33),
+                                   (2, 2048, 300)])
+def test_extreme_shapes(M, K, L, layout):
+    """One-row batches by the thousand, 100k rows of one chunk, long K over
+    tiny batches, one row past an atom block: every output against the oracle."""
+    p = synthetic.make_problem(M, K, L, seed=M * 7 + K + L)
+    ref, sums, sumabs = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
+    got = run(p, M, K, L, layout, via_gpu_repack=(layout == nv.SF_PERMUTED_128x4))
+    parity.assert_parity(got, ref, sums, sumabs, f"M={M} K={K} L={L} layout={layout}")
