@@ -61,6 +61,8 @@ def parse_args():
                     choices=[w[0] for w in synthetic.WORKLOADS])
     ap.add_argument("--ncu", action="store_true",
                     help="only run warmup+steps calls of --workload (for profiler captures)")
+    ap.add_argument("--repack", action="store_true",
+                    help="with --ncu: run the scale repack of --workload's sfa instead of the GEMV")
     return ap.parse_args()
 
 
@@ -165,9 +167,13 @@ def gpu_id_for_smi(torch, dev_index: int) -> str:
 # ---------------------------------------------------------------------------
 
 def kernel_source_hash() -> str:
+    """Hash of the sources the GEMV launch is built from: every file under csrc/
+    except the separate scale-repack kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_block_scaled_gemv_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
+        if name == "repack.cu":
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -476,6 +482,33 @@ def run_native(args):
                                   "single_call_l2_flushed_us": round(smed, 3)}), flush=True)
                 del wprob
                 torch.cuda.empty_cache()
+        # the scale repack (plain -> 128x4 atoms) of each workload's sfa, graph-replayed
+        # over rotating buffers; bytes = plain scales read + permuted atoms written
+        for wname, wM, wK, wL in synthetic.WORKLOADS:
+            wp = synthetic.make_problem(wM, wK, wL, seed=0)
+            src0 = torch.from_numpy(wp["sfa"]).to(dev)
+            out_bytes = nv.nvfp4_permuted_scale_bytes(wM, wK, wL)
+            rbytes = src0.numel() + out_bytes
+            sets = max(2, min(ROTATE_SETS, -(-400 * 2 ** 20 // rbytes)))
+            srcs = [src0.clone() for _ in range(sets)]
+            dsts = [torch.empty(out_bytes, dtype=torch.uint8, device=dev) for _ in range(sets)]
+            del src0
+
+            class _Repack:
+                def call(self, nv_, i, h):
+                    nv_.nvfp4_repack_scales(srcs[i % sets].data_ptr(), dsts[i % sets].data_ptr(),
+                                            wM, wK, wL, h)
+
+            rsteps = max(64, min(20000, int(2e9 / rbytes)) // 64 * 64)
+            rus, _, _ = time_graph(torch, nv, _Repack(), rsteps, 64, stream)
+            gbs = rbytes / (rus * 1e-6) / 1e9
+            print(json.dumps({"workload": wname, "kernel": "repack_scales (sfa)",
+                              "us_per_call": round(rus, 3), "bytes_per_call": rbytes,
+                              "gb_per_s": round(gbs, 1),
+                              "pct_of_hbm_peak": round(100 * gbs / peaks["hbm_gbs"], 2),
+                              "rotating_sets": sets, "calls": rsteps}), flush=True)
+            del srcs, dsts
+            torch.cuda.empty_cache()
         # the extended entry point on the headline shape
         wname, wM, wK, wL = WORKLOAD
         wp = synthetic.make_problem(wM, wK, wL, seed=0)
@@ -505,8 +538,17 @@ def run_profile_case(args):
     name, M, K, L = next(w for w in synthetic.WORKLOADS if w[0] == args.workload)
     layout = nv.SF_PLAIN if args.layout == "plain" else nv.SF_PERMUTED_128x4
     p = synthetic.make_problem(M, K, L, seed=0)
-    prob = DeviceProblem(torch, nv, p, M, K, L, layout, dev, 2)
     stream = torch.cuda.Stream(device=dev)
+    if args.repack:
+        src = torch.from_numpy(p["sfa"]).to(dev)
+        dst = torch.empty(nv.nvfp4_permuted_scale_bytes(M, K, L), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+        for _ in range(args.warmup + args.steps):
+            nv.nvfp4_repack_scales(src.data_ptr(), dst.data_ptr(), M, K, L, stream.cuda_stream)
+        stream.synchronize()
+        print(f"profile case done: {name} sfa repack {args.warmup}+{args.steps} calls")
+        return
+    prob = DeviceProblem(torch, nv, p, M, K, L, layout, dev, 2)
     torch.cuda.synchronize()
     for i in range(args.warmup + args.steps):
         prob.call(nv, i, stream.cuda_stream)

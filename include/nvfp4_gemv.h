@@ -167,7 +167,8 @@ nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa
  * nvfp4_permuted_scale_bytes(rows, K, L) bytes and must not overlap src.
  * Use rows = M for sfa and rows = 1 for sfb.
  * Shapes: rows, L >= 0, K % 64 == 0 (empty is a no-op).
- * Alignment: src 4-byte aligned; dst 16-byte aligned.
+ * Alignment: src 4-byte aligned; dst 16-byte aligned.  With K % 256 == 0 and a
+ * 16-byte aligned src a shared-memory-free kernel runs; the result is the same.
  */
 nvfp4_status_t nvfp4_repack_scales(const void* src, void* dst, int64_t rows, int64_t K,
                                    int64_t L, struct CUstream_st* stream);

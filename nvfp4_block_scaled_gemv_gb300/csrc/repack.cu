@@ -13,6 +13,11 @@
 // loads since plain rows are only 4-byte aligned), staged in shared memory,
 // and written back as whole 512-byte atoms with 16-byte stores.  The grid is
 // sized to the SMs and strides over tiles.
+//
+// When every plain row starts on a 16-byte boundary (K % 256 == 0 and a
+// 16-byte aligned source) a register transpose does the same permutation with
+// no shared memory: one thread reads 16 bytes (4 atom columns) of rows i,
+// 32+i, 64+i, 96+i of a 128-row block and writes position i of those 4 atoms.
 #include <cstdint>
 
 #include "internal.h"
@@ -63,6 +68,39 @@ __global__ void __launch_bounds__(kRepackThreads)
   }
 }
 
+constexpr int kVecThreads = 128;
+
+// Thread u: lanes cover 4 consecutive 16-byte columns of 8 consecutive rows
+// (64 contiguous source bytes per row, 128 contiguous destination bytes per
+// atom and store); warps then step over column groups, the 4 row groups
+// i/8 and finally the (l, 128-row block) pairs.
+__global__ void __launch_bounds__(kVecThreads)
+    repack_scales_vec_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t rows,
+                             int32_t rest_m, int32_t qw, int64_t units) {
+  const int64_t u = (int64_t)blockIdx.x * kVecThreads + threadIdx.x;
+  if (u >= units) return;
+  const int32_t groups = (qw + 3) / 4;  // 4-column groups per row
+  const int ql = (int)(u % 4), il = (int)((u / 4) % 8);
+  const int64_t w = u / 32;
+  const int32_t q = (int32_t)(w % groups) * 4 + ql;
+  if (q >= qw) return;
+  const int i = (int)((w / groups) % 4) * 8 + il;
+  const int64_t blk = w / ((int64_t)groups * 4);  // l * rest_m + m / 128
+  const int64_t l = blk / rest_m;
+  const int64_t m0 = (blk - l * rest_m) * 128 + i;
+  uint4 x[4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const int64_t m = m0 + 32 * g;
+    x[g] = m < rows ? src[(l * rows + m) * qw + q] : make_uint4(0, 0, 0, 0);
+  }
+  uint4* out = dst + (blk * (int64_t)qw * 4 + (int64_t)q * 4) * 32 + i;
+  out[0] = make_uint4(x[0].x, x[1].x, x[2].x, x[3].x);
+  out[32] = make_uint4(x[0].y, x[1].y, x[2].y, x[3].y);
+  out[64] = make_uint4(x[0].z, x[1].z, x[2].z, x[3].z);
+  out[96] = make_uint4(x[0].w, x[1].w, x[2].w, x[3].w);
+}
+
 }  // namespace
 
 cudaError_t repack_ctas_per_sm(int* out) {
@@ -74,6 +112,18 @@ cudaError_t launch_repack(const uint8_t* src, uint8_t* dst, int64_t rows, int64_
                           int64_t max_ctas, cudaStream_t stream) {
   const int32_t rest_m = (int32_t)((rows + 127) / 128);
   const int32_t rest_k = (int32_t)(K / 64);
+  const int32_t qw = rest_k / 4;
+  const int64_t units = L * rest_m * 32 * (int64_t)((qw + 3) / 4) * 4;
+  if (rest_k % 4 == 0 && reinterpret_cast<uintptr_t>(src) % 16 == 0 &&
+      units <= (int64_t)0x7fffffff * kVecThreads) {
+    if (units == 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((units + kVecThreads - 1) / kVecThreads), 1, 1);
+    cfg.blockDim = dim3(kVecThreads, 1, 1);
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, repack_scales_vec_kernel, reinterpret_cast<const uint4*>(src),
+                              reinterpret_cast<uint4*>(dst), rows, rest_m, qw, units);
+  }
   const int64_t tiles = L * rest_m * ((rest_k + kTileCols - 1) / kTileCols);
   if (tiles == 0) return cudaSuccess;
   const int64_t cap = max_ctas > 0 ? max_ctas : 1;
