@@ -61,6 +61,9 @@ def parse_args():
                     choices=[w[0] for w in synthetic.WORKLOADS])
     ap.add_argument("--ncu", action="store_true",
                     help="only run warmup+steps calls of --workload (for profiler captures)")
+    ap.add_argument("--schedule", default=None,
+                    help="with --ncu: KERNEL,LANES_PER_ROW,K_SPLIT,CTAS for nvfp4_gemv_explicit "
+                         "instead of the chosen schedule")
     ap.add_argument("--repack", action="store_true",
                     help="with --ncu: run the scale repack of --workload's sfa instead of the GEMV")
     return ap.parse_args()
@@ -167,12 +170,12 @@ def gpu_id_for_smi(torch, dev_index: int) -> str:
 # ---------------------------------------------------------------------------
 
 def kernel_source_hash() -> str:
-    """Hash of the sources the GEMV launch is built from: every file under csrc/
-    except the separate scale-repack kernel."""
+    """Hash of the sources the default GEMV launch is built from: every file under
+    csrc/ except the separate scale-repack and tensor-core kernels."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_block_scaled_gemv_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name == "repack.cu":
+        if name in ("repack.cu", "gemv_tc.cu"):
             continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
@@ -550,8 +553,15 @@ def run_profile_case(args):
         return
     prob = DeviceProblem(torch, nv, p, M, K, L, layout, dev, 2)
     torch.cuda.synchronize()
+    sched = [int(v) for v in args.schedule.split(",")] if args.schedule else None
     for i in range(args.warmup + args.steps):
-        prob.call(nv, i, stream.cuda_stream)
+        if sched is None:
+            prob.call(nv, i, stream.cuda_stream)
+        else:
+            s = prob.sets[i % len(prob.sets)]
+            nv.nvfp4_gemv_explicit(s["a"].data_ptr(), s["b"].data_ptr(), s["sfa"].data_ptr(),
+                                   s["sfb"].data_ptr(), s["c"].data_ptr(), M, K, L, layout,
+                                   *sched, stream=stream.cuda_stream)
     stream.synchronize()
     print(f"profile case done: {name} {args.layout} {args.warmup}+{args.steps} calls")
 

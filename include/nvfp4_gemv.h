@@ -132,7 +132,7 @@ nvfp4_status_t nvfp4_gemv_ex(const void* a, const void* b, const void* sfa, cons
                              void* c, int64_t M, int64_t K, int64_t L, int sf_layout,
                              const nvfp4_gemv_options_t* options, struct CUstream_st* stream);
 
-/* The two GEMV kernels (same arithmetic, different data movement). */
+/* The GEMV kernels (CUDA-core kernels 0 and 1 share their arithmetic). */
 typedef enum {
   /* Warps load up to 8 rows' 32-byte K chunks straight into registers with
    * 256-bit loads, then compute. */
@@ -141,7 +141,17 @@ typedef enum {
    * per-warp shared-memory ring with cp.async, so every warp keeps two tasks
    * in flight while it computes one.  The default for every K > 0; needs
    * k_split no larger than the K steps, ceil(K/64 / lanes_per_row). */
-  NVFP4_KERNEL_PIPELINED = 1
+  NVFP4_KERNEL_PIPELINED = 1,
+  /* The tensor cores' block-scaled MMA (tcgen05 kind::mxf4nvf4, 16-element
+   * E4M3 blocks, M = 128 tiles, b padded to N = 16 with zero rows), fed by
+   * TMA; pre-permuted scales only (the 128x4 atom is the MMA's scale
+   * layout).  k_split = CTAs per cluster (1, 2, 4 or 8, at most ceil(K/256))
+   * splitting each tile's K range, summed in cluster rank order through
+   * distributed shared memory; ctas a multiple of k_split (the clusters are
+   * persistent over the L*ceil(M/128) tiles); lanes_per_row is ignored.
+   * The MMA sums in fp32 in an order of its own: c meets the same accuracy
+   * contract, not the CUDA-core kernels' bits. */
+  NVFP4_KERNEL_TENSOR = 2
 } nvfp4_kernel_t;
 
 /*
@@ -183,6 +193,13 @@ const char* nvfp4_status_string(int status);
 /* The cudaError_t of the most recent NVFP4_ERR_CUDA on the calling thread
  * (0 if none). */
 int nvfp4_last_cuda_error(void);
+
+/* Waits of the tensor-core kernel that gave up: every wait of that kernel on
+ * a pipeline barrier is bounded (2 s), and a wait that runs out is counted
+ * here and makes its thread skip the rest of its work (the launch's c is
+ * then not valid).  Synchronises the device; reset != 0 clears the count
+ * after reading it.  Returns the count, or -1 on a CUDA error. */
+int nvfp4_tensor_wait_timeouts(int reset);
 
 /*
  * Launch plan of nvfp4_gemv, computed on the host only (no GPU needed), for

@@ -37,6 +37,7 @@ EXPORTS = (
     "nvfp4_status_string",
     "nvfp4_last_cuda_error",
     "nvfp4_gemv_plan",
+    "nvfp4_tensor_wait_timeouts",
 )
 
 
@@ -54,6 +55,7 @@ class Nvfp4Error(RuntimeError):
 
 KERNEL_DIRECT = 0
 KERNEL_PIPELINED = 1
+KERNEL_TENSOR = 2
 
 
 class _Plan(ctypes.Structure):
@@ -96,6 +98,8 @@ def library() -> ctypes.CDLL:
     lib.nvfp4_last_cuda_error.restype = I
     lib.nvfp4_gemv_plan.argtypes = [I64, I64, I64, I, I, I, I, ctypes.POINTER(_Plan)]
     lib.nvfp4_gemv_plan.restype = I
+    lib.nvfp4_tensor_wait_timeouts.argtypes = [I]
+    lib.nvfp4_tensor_wait_timeouts.restype = I
     _lib = lib
     return lib
 
@@ -145,6 +149,11 @@ def nvfp4_permuted_scale_bytes(rows: int, K: int, L: int) -> int:
 
 def nvfp4_last_cuda_error() -> int:
     return int(library().nvfp4_last_cuda_error())
+
+
+def nvfp4_tensor_wait_timeouts(reset: bool = False) -> int:
+    """Bounded waits of the tensor-core kernel that ran out (synchronises)."""
+    return int(library().nvfp4_tensor_wait_timeouts(1 if reset else 0))
 
 
 def nvfp4_gemv_plan(M: int, K: int, L: int, sf_layout: int = SF_PLAIN, num_sms: int = 152,

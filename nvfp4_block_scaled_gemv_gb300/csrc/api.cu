@@ -140,7 +140,9 @@ nvfp4_status_t run_gemv(const void* a, const void* b, const void* sfa, const voi
   const bool permuted = sf_layout == NVFP4_SF_PERMUTED_128x4;
   const GemvParams p = make_params(a, b, sfa, sfb, c, M, K, L, permuted, plan, opt);
   cudaError_t err;
-  if (plan.kernel == kKernelAsync)
+  if (plan.kernel == kKernelTensor)
+    err = launch_gemv_tc(p, L, plan.k_split, plan.ctas, stream);
+  else if (plan.kernel == kKernelAsync)
     err = permuted ? launch_async_permuted(p, plan, stream) : launch_async_plain(p, plan, stream);
   else
     err = permuted ? launch_gemv_permuted(p, plan, stream) : launch_gemv_plain(p, plan, stream);
@@ -327,7 +329,8 @@ nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa
                                    int64_t ctas, struct CUstream_st* stream) {
   nvfp4_status_t st = validate_gemv_shape(M, K, L, sf_layout);
   if (st != NVFP4_OK) return st;
-  if (kernel != kKernelDirect && kernel != kKernelAsync) return NVFP4_ERR_INVALID_VALUE;
+  if (kernel != kKernelDirect && kernel != kKernelAsync && kernel != kKernelTensor)
+    return NVFP4_ERR_INVALID_VALUE;
   if (lanes_per_row != 4 && lanes_per_row != 8 && lanes_per_row != 16 && lanes_per_row != 32)
     return NVFP4_ERR_INVALID_VALUE;
   if (k_split != 1 && k_split != 2 && k_split != 4 && k_split != 8) return NVFP4_ERR_INVALID_VALUE;
@@ -335,6 +338,13 @@ nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa
   const int64_t steps = (K / 64 + lanes_per_row - 1) / lanes_per_row;
   // the pipelined kernel needs a K range and a step for every K-split warp
   if (kernel == kKernelAsync && (K == 0 || k_split > steps)) return NVFP4_ERR_INVALID_VALUE;
+  // the tensor-core kernel: pre-permuted scales, clusters of k_split CTAs that
+  // each take at least one 256-element K stage of every 128-row tile
+  if (kernel == kKernelTensor) {
+    if (sf_layout != NVFP4_SF_PERMUTED_128x4 || K == 0) return NVFP4_ERR_INVALID_VALUE;
+    if (k_split > (K + 255) / 256 || ctas % k_split != 0) return NVFP4_ERR_INVALID_VALUE;
+    if (L * ((M + 127) / 128) > 0x7fffffff) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  }
   if (M == 0 || L == 0) return NVFP4_OK;
   st = validate_gemv_pointers(a, b, sfa, sfb, c, K);
   if (st != NVFP4_OK) return st;
@@ -387,6 +397,17 @@ const char* nvfp4_status_string(int status) {
 }
 
 int nvfp4_last_cuda_error(void) { return g_last_cuda_error; }
+
+int nvfp4_tensor_wait_timeouts(int reset) {
+  int v = 0;
+  const cudaError_t err = tc_wait_timeouts(reset, &v);
+  if (err != cudaSuccess) {
+    g_last_cuda_error = (int)err;
+    (void)cudaGetLastError();
+    return -1;
+  }
+  return v;
+}
 
 nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, int kernel,
                                int num_sms, int ctas_per_sm, nvfp4_gemv_plan_t* out) {

@@ -19,7 +19,7 @@ constexpr int kAsyncStages = 3;
 constexpr int kAsyncStageBytes = kAsyncItems * (32 * 32 + 32 * 4);
 constexpr int kAsyncSmemBytes = kGemvWarps * kAsyncStages * kAsyncStageBytes;
 
-enum KernelKind { kKernelDirect = 0, kKernelAsync = 1 };
+enum KernelKind { kKernelDirect = 0, kKernelAsync = 1, kKernelTensor = 2 };
 
 // Everything a GEMV kernel needs, by value (kernel parameter space).
 struct GemvParams {
@@ -75,6 +75,16 @@ cudaError_t gemv_ctas_per_sm(int* out);
 cudaError_t repack_ctas_per_sm(int* out);
 cudaError_t launch_repack(const uint8_t* src, uint8_t* dst, int64_t rows, int64_t K, int64_t L,
                           int64_t max_ctas, cudaStream_t stream);
+
+// Tensor-core GEMV (gemv_tc.cu, pre-permuted scales): ctas CTAs in clusters
+// of ks, each cluster splitting a 128-row tile's K range ks ways.
+cudaError_t launch_gemv_tc(const GemvParams& p, int64_t L, int ks, int64_t ctas,
+                           cudaStream_t stream);
+// Clusters of ks tensor-core CTAs that can be resident at once.
+cudaError_t tc_max_active_clusters(int ks, int* out);
+// Bounded waits of the tensor-core kernel that gave up (read, then optionally
+// cleared; synchronous).
+cudaError_t tc_wait_timeouts(int reset, int* out);
 
 // Per-layout GEMV launchers (gemv_plain.cu, gemv_permuted.cu).
 cudaError_t launch_gemv_plain(const GemvParams& p, const GemvPlan& plan, cudaStream_t stream);

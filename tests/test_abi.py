@@ -93,6 +93,24 @@ def test_explicit_schedule_validation(lib):
     assert lib.nvfp4_gemv_explicit(*zero_k, nv.KERNEL_PIPELINED, 32, 1, 1, None) == nv.ERR_INVALID_VALUE
 
 
+def test_tensor_kernel_schedule_validation(lib):
+    # (a, b, sfa, sfb, c, M, K, L, layout): checked before any CUDA call
+    perm = (64, 64, 64, 64, 64, 300, 1024, 2, nv.SF_PERMUTED_128x4)
+    plain = perm[:-1] + (nv.SF_PLAIN,)
+    T = nv.KERNEL_TENSOR
+    # pre-permuted scales only
+    assert lib.nvfp4_gemv_explicit(*plain, T, 4, 1, 1, None) == nv.ERR_INVALID_VALUE
+    # every CTA of a cluster needs a 256-element K stage: K = 1024 has 4
+    assert lib.nvfp4_gemv_explicit(*perm, T, 4, 8, 8, None) == nv.ERR_INVALID_VALUE
+    # whole clusters only
+    assert lib.nvfp4_gemv_explicit(*perm, T, 4, 2, 3, None) == nv.ERR_INVALID_VALUE
+    assert lib.nvfp4_gemv_explicit(*perm, T, 4, 3, 3, None) == nv.ERR_INVALID_VALUE
+    zero_k = perm[:6] + (0,) + perm[7:]
+    assert lib.nvfp4_gemv_explicit(*zero_k, T, 4, 1, 1, None) == nv.ERR_INVALID_VALUE
+    # empty problems are no-ops
+    assert lib.nvfp4_gemv_explicit(*(perm[:5] + (0,) + perm[6:]), T, 4, 1, 1, None) == nv.OK
+
+
 def test_repack_validation(lib):
     assert lib.nvfp4_repack_scales(64, 64, -1, 64, 1, None) == nv.ERR_INVALID_VALUE
     assert lib.nvfp4_repack_scales(64, 64, 4, 80, 1, None) == nv.ERR_UNSUPPORTED_SHAPE

@@ -1,0 +1,114 @@
+"""GPU parity of the tensor-core kernel (NVFP4_KERNEL_TENSOR) against the CPU oracle.
+
+The kernel takes pre-permuted scales only.  Every launch is checked for
+writes outside c (sentinel slack) and for bounded pipeline waits that ran out
+(nvfp4_tensor_wait_timeouts must stay 0).  Tolerance as for the CUDA-core
+kernels: |gpu - oracle| <= 1e-3 * sum|terms| + 1 fp16 ulp of the oracle value.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import nvfp4_block_scaled_gemv_gb300 as nv  # noqa: E402
+import oracle  # noqa: E402
+from nvfp4_block_scaled_gemv_gb300 import build as libbuild  # noqa: E402
+from nvfp4_block_scaled_gemv_gb300 import synthetic  # noqa: E402
+from oracle import parity  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+SENTINEL = -4096.0
+SENTINEL_BITS = int(np.array([SENTINEL], dtype=np.float16).view(np.uint16)[0])
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    libbuild.build()
+    nv.library()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    nv.nvfp4_tensor_wait_timeouts(reset=True)
+
+
+def to_dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+
+
+def run_tc(a, b, sfa_plain, sfb_plain, M, K, L, ks, ctas):
+    """One tensor-core launch on oracle-repacked scales; returns c's fp16 bits [L, M]."""
+    sfa = to_dev(oracle.repack_scales(sfa_plain, M, K, L))
+    sfb = to_dev(oracle.repack_scales(np.asarray(sfb_plain).reshape(L, 1, K // 16), 1, K, L))
+    ad, bd = to_dev(a), to_dev(b)
+    pad = 64
+    buf = torch.full((L * M + 2 * pad,), SENTINEL, dtype=torch.float16, device=DEV)
+    c = buf[pad:pad + L * M]
+    nv.nvfp4_gemv_explicit(ad.data_ptr(), bd.data_ptr(), sfa.data_ptr(), sfb.data_ptr(),
+                           c.data_ptr(), M, K, L, nv.SF_PERMUTED_128x4, nv.KERNEL_TENSOR, 4, ks,
+                           ctas, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_tensor_wait_timeouts(reset=True) == 0, "a pipeline wait ran out"
+    whole = buf.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert np.all(whole[:pad] == SENTINEL_BITS) and np.all(whole[pad + L * M:] == SENTINEL_BITS), \
+        "write outside c"
+    return whole[pad:pad + L * M].reshape(L, M)
+
+
+def check(p, M, K, L, ks, ctas):
+    ref, sums, sumabs = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
+    got = run_tc(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L, ks, ctas)
+    parity.assert_parity(got, ref, sums, sumabs, f"tensor M={M} K={K} L={L} ks={ks} ctas={ctas}")
+    return got
+
+
+def test_all_ones():
+    # a = b = 1.0 (E2M1 code 2), every scale 1.0 (E4M3 0x38): c = K exactly
+    M, K, L = 128, 256, 1
+    a = np.full((L, M, K // 2), 0x22, np.uint8)
+    b = np.full((L, K // 2), 0x22, np.uint8)
+    s = np.full((L, M, K // 16), 0x38, np.uint8)
+    got = run_tc(a, b, s, s[:, 0, :], M, K, L, 1, 1)
+    assert np.all(got.view(np.float16) == K)
+
+
+def test_row_sums():
+    # b = 1.0 and unit scales: c[m] is the plain sum of row m's E2M1 values
+    M, K, L = 200, 1088, 2
+    rng = np.random.default_rng(7)
+    p = {"a": rng.integers(0, 256, (L, M, K // 2), dtype=np.uint8),
+         "b": np.full((L, K // 2), 0x22, np.uint8),
+         "sfa": np.full((L, M, K // 16), 0x38, np.uint8),
+         "sfb": np.full((L, K // 16), 0x38, np.uint8)}
+    check(p, M, K, L, 2, 4)
+
+
+# (M, K, L, k_split, ctas): one CTA; ragged M; a last K stage of 1..3 MMAs;
+# clusters of 2, 4 and 8 (split K summed through distributed shared memory);
+# fewer clusters than tiles (persistent clusters); a 128-row block per batch
+TC_CASES = [
+    (128, 256, 1, 1, 1), (1, 64, 1, 1, 1), (7, 192, 3, 1, 2), (256, 512, 2, 1, 2),
+    (200, 1088, 3, 1, 3), (129, 320, 2, 2, 2), (256, 2048, 2, 2, 2), (200, 1088, 3, 2, 4),
+    (1000, 4096, 2, 4, 8), (333, 16384, 1, 8, 16), (513, 2304, 2, 8, 8), (640, 768, 5, 2, 6),
+    (4096, 1024, 1, 4, 152), (128, 16384, 4, 8, 32),
+]
+
+
+@pytest.mark.parametrize("M,K,L,ks,ctas", TC_CASES)
+def test_parity_tensor_kernel(M, K, L, ks, ctas):
+    p = synthetic.make_problem(M, K, L, seed=M + K + ks)
+    check(p, M, K, L, ks, ctas)
+
+
+def test_tensor_kernel_is_deterministic():
+    M, K, L = 1000, 4096, 2
+    p = synthetic.make_problem(M, K, L, seed=5)
+    first = check(p, M, K, L, 4, 8)
+    again = run_tc(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L, 4, 8)
+    assert np.array_equal(first, again)
+
+
+@pytest.mark.parametrize("name,ks,ctas", [("M7168_K2048_L4", 2, 152), ("M7168_K16384_L1", 8, 152)])
+def test_tensor_kernel_full_size(name, ks, ctas):
+    _, M, K, L = next(w for w in synthetic.WORKLOADS if w[0] == name)
+    p = synthetic.make_problem(M, K, L, seed=0)
+    check(p, M, K, L, ks, ctas)
