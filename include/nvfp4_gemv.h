@@ -148,7 +148,8 @@ typedef enum {
    * layout).  k_split = CTAs per cluster (1, 2, 4 or 8, at most ceil(K/256))
    * splitting each tile's K range, summed in cluster rank order through
    * distributed shared memory; ctas a multiple of k_split (the clusters are
-   * persistent over the L*ceil(M/128) tiles); lanes_per_row is ignored.
+   * persistent over the L*ceil(M/128) tiles); lanes_per_row = pipeline
+   * stages per CTA (2 or 4: 4, 3 or 2 CTAs of 2 stages share an SM, 2 of 4).
    * The MMA sums in fp32 in an order of its own: c meets the same accuracy
    * contract, not the CUDA-core kernels' bits. */
   NVFP4_KERNEL_TENSOR = 2
@@ -168,6 +169,42 @@ nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa
                                    const void* sfb, void* c, int64_t M, int64_t K, int64_t L,
                                    int sf_layout, int kernel, int lanes_per_row, int k_split,
                                    int64_t ctas, struct CUstream_st* stream);
+
+/*
+ * Small-N NVFP4 GEMM (a decode batch of N <= 16 vectors per batch): for each
+ * batch l, vector n < N and row m,
+ *   c[l][n][m] = fp16(alpha * sum_k E2M1(a[m,k,l]) * E4M3(sfa[m,k/16,l])
+ *                                   * E2M1(b[n,k,l]) * E4M3(sfb[n,k/16,l]) + bias[l][n][m]),
+ * N GEMVs that share one pass over A.  (Submission 103289's
+ * `cute_jit_kernel` gives b a stride of 128 padded columns, made for
+ * torch._scaled_mm; here b has the N rows given.)
+ * Layouts: a [L][M][K/2] as for nvfp4_gemv; b [L][N][K/2], row n of batch l
+ * at b + l*b_batch_stride + n*K/2 (b_batch_stride 0 = N*K/2); scales
+ * pre-permuted only: sfa as for nvfp4_gemv, sfb the permuted form of
+ * [L][N][K/16] (one 128-row atom block per batch, rows 0..N-1:
+ * nvfp4_repack_scales with rows = N), batch stride sfb_batch_stride
+ * (0 = (K/64)*512); c fp16 [L][N][M]; bias fp16 [L][N][M] or NULL.
+ * N = 1 is nvfp4_gemv_ex with permuted scales (the CUDA-core GEMV); N >= 2
+ * runs the tensor-core kernel (NVFP4_KERNEL_TENSOR), whose cost does not grow
+ * with N.  Shapes: M, L >= 0, 0 <= N <= 16 (N > 16: UNSUPPORTED_SHAPE),
+ * K % 64 == 0 (K = 0 gives c = fp16(bias) or zeros).  Alignment: a, b, sfa,
+ * sfb 32 bytes; c and bias 2 bytes; batch strides as for nvfp4_gemv_ex.
+ */
+nvfp4_status_t nvfp4_gemm_small_n(const void* a, const void* b, const void* sfa, const void* sfb,
+                                  void* c, int64_t M, int64_t N, int64_t K, int64_t L,
+                                  const nvfp4_gemv_options_t* options, struct CUstream_st* stream);
+
+/*
+ * nvfp4_gemm_small_n (N >= 1, always the tensor-core kernel, default options)
+ * with its schedule given: stages (2 or 4) pipeline stages per CTA, k_split
+ * (1, 2, 4 or 8, at most ceil(K/256); 1 when K = 0) CTAs per cluster
+ * splitting each 128-row tile's K range, ctas in [1, 2^31) a multiple of
+ * k_split.  Invalid values give NVFP4_ERR_INVALID_VALUE.
+ */
+nvfp4_status_t nvfp4_gemm_small_n_explicit(const void* a, const void* b, const void* sfa,
+                                           const void* sfb, void* c, int64_t M, int64_t N,
+                                           int64_t K, int64_t L, int stages, int k_split,
+                                           int64_t ctas, struct CUstream_st* stream);
 
 /*
  * Scale repack: plain [L][rows][K/16] E4M3 -> the 128x4-atom pre-permuted

@@ -38,6 +38,8 @@ EXPORTS = (
     "nvfp4_last_cuda_error",
     "nvfp4_gemv_plan",
     "nvfp4_tensor_wait_timeouts",
+    "nvfp4_gemm_small_n",
+    "nvfp4_gemm_small_n_explicit",
 )
 
 
@@ -98,6 +100,11 @@ def library() -> ctypes.CDLL:
     lib.nvfp4_last_cuda_error.restype = I
     lib.nvfp4_gemv_plan.argtypes = [I64, I64, I64, I, I, I, I, ctypes.POINTER(_Plan)]
     lib.nvfp4_gemv_plan.restype = I
+    lib.nvfp4_gemm_small_n.argtypes = [P, P, P, P, P, I64, I64, I64, I64,
+                                       ctypes.POINTER(_Options), P]
+    lib.nvfp4_gemm_small_n.restype = I
+    lib.nvfp4_gemm_small_n_explicit.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I, I, I64, P]
+    lib.nvfp4_gemm_small_n_explicit.restype = I
     lib.nvfp4_tensor_wait_timeouts.argtypes = [I]
     lib.nvfp4_tensor_wait_timeouts.restype = I
     _lib = lib
@@ -136,6 +143,25 @@ def nvfp4_gemv_explicit(a: int, b: int, sfa: int, sfb: int, c: int, M: int, K: i
     _check(library().nvfp4_gemv_explicit(a, b, sfa, sfb, c, M, K, L, sf_layout, kernel,
                                          lanes_per_row, k_split, ctas, stream),
            "nvfp4_gemv_explicit")
+
+
+def nvfp4_gemm_small_n(a: int, b: int, sfa: int, sfb: int, c: int, M: int, N: int, K: int,
+                       L: int, alpha: float = 1.0, bias: int = 0, b_batch_stride: int = 0,
+                       sfb_batch_stride: int = 0, stream: int = 0) -> None:
+    """Small-N GEMM: c [L][N][M] from a [L][M][K/2], b [L][N][K/2] and
+    pre-permuted scales (sfb: the permuted form of [L][N][K/16])."""
+    opt = _Options(alpha, bias or None, b_batch_stride, sfb_batch_stride)
+    _check(library().nvfp4_gemm_small_n(a, b, sfa, sfb, c, M, N, K, L, ctypes.byref(opt),
+                                        stream), "nvfp4_gemm_small_n")
+
+
+def nvfp4_gemm_small_n_explicit(a: int, b: int, sfa: int, sfb: int, c: int, M: int, N: int,
+                                K: int, L: int, stages: int, k_split: int, ctas: int,
+                                stream: int = 0) -> None:
+    """nvfp4_gemm_small_n on the tensor-core kernel with a given schedule."""
+    _check(library().nvfp4_gemm_small_n_explicit(a, b, sfa, sfb, c, M, N, K, L, stages,
+                                                 k_split, ctas, stream),
+           "nvfp4_gemm_small_n_explicit")
 
 
 def nvfp4_repack_scales(src: int, dst: int, rows: int, K: int, L: int, stream: int = 0) -> None:

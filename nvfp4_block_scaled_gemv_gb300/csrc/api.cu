@@ -16,6 +16,10 @@ std::atomic<int> g_sms[kMaxDevices];
 std::atomic<int> g_gemv_occ[kMaxDevices];
 std::atomic<int> g_repack_occ[kMaxDevices];
 
+// Resident clusters of the tensor-core kernel per device, stage count (2, 4),
+// column count (1, 2, 4, 8, 16) and cluster size (1, 2, 4, 8); 0 = not queried.
+std::atomic<int> g_tc_clusters[kMaxDevices][2][5][4];
+
 constexpr int64_t kMaxK = int64_t(1) << 30;
 constexpr int64_t kMaxRows = int64_t(1) << 40;  // M * L
 constexpr int64_t kMaxM = (int64_t(1) << 31) - 1;
@@ -141,11 +145,108 @@ nvfp4_status_t run_gemv(const void* a, const void* b, const void* sfa, const voi
   const GemvParams p = make_params(a, b, sfa, sfb, c, M, K, L, permuted, plan, opt);
   cudaError_t err;
   if (plan.kernel == kKernelTensor)
-    err = launch_gemv_tc(p, L, plan.k_split, plan.ctas, stream);
+    err = launch_gemv_tc(p, 1, L, K / 2, plan.lanes_per_row, plan.k_split, plan.ctas, stream);
   else if (plan.kernel == kKernelAsync)
     err = permuted ? launch_async_permuted(p, plan, stream) : launch_async_plain(p, plan, stream);
   else
     err = permuted ? launch_gemv_permuted(p, plan, stream) : launch_gemv_plain(p, plan, stream);
+  if (err != cudaSuccess) return cuda_failure(err);
+  return NVFP4_OK;
+}
+
+int log2_small(int64_t v) {  // v in {1, 2, 4, 8, 16}
+  int r = 0;
+  while ((int64_t(1) << r) < v) ++r;
+  return r;
+}
+
+// Clusters of ks tensor-core CTAs (stages, N columns) resident at once on the
+// current device, cached.
+cudaError_t tc_resident_clusters(int stages, int64_t N, int ks, int* out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const int nc = N <= 1 ? 1 : N <= 2 ? 2 : N <= 4 ? 4 : N <= 8 ? 8 : 16;
+  std::atomic<int>& slot = g_tc_clusters[dev][stages == 4 ? 1 : 0][log2_small(nc)][log2_small(ks)];
+  int v = slot.load(std::memory_order_relaxed);
+  if (v <= 0) {
+    err = tc_max_active_clusters(stages, N, ks, &v);
+    if (err != cudaSuccess) return err;
+    if (v < 1) v = 1;
+    slot.store(v, std::memory_order_relaxed);
+  }
+  *out = v;
+  return cudaSuccess;
+}
+
+// Tensor-core schedule: 2 stages per CTA (the most CTAs per SM, whose copy and
+// MMA chains overlap), and the cluster size that minimises the K stages of
+// the busiest CTA when the clusters that fit at once share the L*ceil(M/128)
+// tiles; ties go to the smaller cluster.
+cudaError_t plan_tc(int64_t M, int64_t N, int64_t K, int64_t L, int* stages, int* k_split,
+                    int64_t* ctas) {
+  const int64_t tiles = L * ((M + 127) / 128);
+  const int64_t kst = (K + 255) / 256;
+  *stages = 2;
+  *k_split = 1;
+  *ctas = 1;
+  double best = -1.0;
+  for (int ks = 1; ks <= 8; ks *= 2) {
+    if (ks > 1 && ks > kst) break;
+    int resident = 0;
+    const cudaError_t err = tc_resident_clusters(2, N, ks, &resident);
+    if (err != cudaSuccess) return err;
+    const int64_t clusters = tiles < resident ? tiles : resident;
+    const int64_t per_cluster = (tiles + clusters - 1) / clusters;
+    const int64_t per_cta = (kst + ks - 1) / ks;
+    const double cost = (double)(per_cluster * (per_cta > 0 ? per_cta : 1));
+    if (best < 0.0 || cost < best - 1e-9) {
+      best = cost;
+      *k_split = ks;
+      *ctas = clusters * ks;
+    }
+  }
+  return cudaSuccess;
+}
+
+// Checks of the small-N GEMM arguments shared by both entry points.
+nvfp4_status_t validate_gemm(const void* a, const void* b, const void* sfa, const void* sfb,
+                             const void* c, int64_t M, int64_t N, int64_t K, int64_t L,
+                             const nvfp4_gemv_options_t& o) {
+  if (M < 0 || N < 0 || K < 0 || L < 0) return NVFP4_ERR_INVALID_VALUE;
+  if (K % 64 != 0 || N > 16) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (K > kMaxK || M > kMaxM) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (M != 0 && L > kMaxRows / M) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (L * ((M + 127) / 128) > 0x7fffffff) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (o.b_batch_stride < 0 || o.sfb_batch_stride < 0) return NVFP4_ERR_INVALID_VALUE;
+  if (o.b_batch_stride != 0 && o.b_batch_stride < N * (K / 2)) return NVFP4_ERR_INVALID_VALUE;
+  if (o.sfb_batch_stride != 0 && o.sfb_batch_stride < (K / 64) * 512) return NVFP4_ERR_INVALID_VALUE;
+  if (o.b_batch_stride % 32 != 0 || o.sfb_batch_stride % 16 != 0) return NVFP4_ERR_MISALIGNED;
+  if (M == 0 || N == 0 || L == 0) return NVFP4_OK;
+  if (c == nullptr) return NVFP4_ERR_INVALID_VALUE;
+  if (K > 0 && (a == nullptr || b == nullptr || sfa == nullptr || sfb == nullptr))
+    return NVFP4_ERR_INVALID_VALUE;
+  if (!aligned(c, 2) || (o.bias != nullptr && !aligned(o.bias, 2))) return NVFP4_ERR_MISALIGNED;
+  if (K > 0 && (!aligned(a, 32) || !aligned(b, 32) || !aligned(sfa, 32) || !aligned(sfb, 32)))
+    return NVFP4_ERR_MISALIGNED;
+  return NVFP4_OK;
+}
+
+nvfp4_status_t run_gemm_tc(const void* a, const void* b, const void* sfa, const void* sfb,
+                           void* c, int64_t M, int64_t N, int64_t K, int64_t L, int stages,
+                           int ks, int64_t ctas, const nvfp4_gemv_options_t& opt,
+                           cudaStream_t stream) {
+  GemvPlan plan;
+  plan.kernel = kKernelTensor;
+  plan.lanes_per_row = stages;
+  plan.k_split = ks;
+  plan.groups = 1;
+  plan.ctas = ctas;
+  plan.steps = 1;
+  GemvParams p = make_params(a, b, sfa, sfb, c, M, K, L, true, plan, opt);
+  if (opt.b_batch_stride == 0) p.b_stride = N * (K / 2);
+  const cudaError_t err = launch_gemv_tc(p, N, L, K / 2, stages, ks, ctas, stream);
   if (err != cudaSuccess) return cuda_failure(err);
   return NVFP4_OK;
 }
@@ -331,7 +432,10 @@ nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa
   if (st != NVFP4_OK) return st;
   if (kernel != kKernelDirect && kernel != kKernelAsync && kernel != kKernelTensor)
     return NVFP4_ERR_INVALID_VALUE;
-  if (lanes_per_row != 4 && lanes_per_row != 8 && lanes_per_row != 16 && lanes_per_row != 32)
+  // lanes per row; for the tensor-core kernel, pipeline stages per CTA
+  if (kernel == kKernelTensor ? (lanes_per_row != 2 && lanes_per_row != 4)
+                              : (lanes_per_row != 4 && lanes_per_row != 8 &&
+                                 lanes_per_row != 16 && lanes_per_row != 32))
     return NVFP4_ERR_INVALID_VALUE;
   if (k_split != 1 && k_split != 2 && k_split != 4 && k_split != 8) return NVFP4_ERR_INVALID_VALUE;
   if (ctas < 1 || ctas > 0x7fffffff) return NVFP4_ERR_INVALID_VALUE;
@@ -394,6 +498,36 @@ const char* nvfp4_status_string(int status) {
     case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA";
     default: return "NVFP4_ERR_UNKNOWN";
   }
+}
+
+nvfp4_status_t nvfp4_gemm_small_n(const void* a, const void* b, const void* sfa, const void* sfb,
+                                  void* c, int64_t M, int64_t N, int64_t K, int64_t L,
+                                  const nvfp4_gemv_options_t* options, struct CUstream_st* stream) {
+  const nvfp4_gemv_options_t& opt = options ? *options : kDefaultOptions;
+  nvfp4_status_t st = validate_gemm(a, b, sfa, sfb, c, M, N, K, L, opt);
+  if (st != NVFP4_OK || M == 0 || N == 0 || L == 0) return st;
+  if (N == 1)
+    return nvfp4_gemv_ex(a, b, sfa, sfb, c, M, K, L, NVFP4_SF_PERMUTED_128x4, &opt, stream);
+  int stages = 2, ks = 1;
+  int64_t ctas = 1;
+  const cudaError_t err = plan_tc(M, N, K, L, &stages, &ks, &ctas);
+  if (err != cudaSuccess) return cuda_failure(err);
+  return run_gemm_tc(a, b, sfa, sfb, c, M, N, K, L, stages, ks, ctas, opt, (cudaStream_t)stream);
+}
+
+nvfp4_status_t nvfp4_gemm_small_n_explicit(const void* a, const void* b, const void* sfa,
+                                           const void* sfb, void* c, int64_t M, int64_t N,
+                                           int64_t K, int64_t L, int stages, int k_split,
+                                           int64_t ctas, struct CUstream_st* stream) {
+  nvfp4_status_t st = validate_gemm(a, b, sfa, sfb, c, M, N, K, L, kDefaultOptions);
+  if (st != NVFP4_OK) return st;
+  if (stages != 2 && stages != 4) return NVFP4_ERR_INVALID_VALUE;
+  if (k_split != 1 && k_split != 2 && k_split != 4 && k_split != 8) return NVFP4_ERR_INVALID_VALUE;
+  if (k_split > 1 && k_split > (K + 255) / 256) return NVFP4_ERR_INVALID_VALUE;
+  if (ctas < 1 || ctas > 0x7fffffff || ctas % k_split != 0) return NVFP4_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0 || L == 0) return NVFP4_OK;
+  return run_gemm_tc(a, b, sfa, sfb, c, M, N, K, L, stages, k_split, ctas, kDefaultOptions,
+                     (cudaStream_t)stream);
 }
 
 int nvfp4_last_cuda_error(void) { return g_last_cuda_error; }

@@ -1,31 +1,36 @@
-// NVFP4 block-scaled batched GEMV on the tensor cores (tcgen05, sm_103a),
-// pre-permuted scales only.
+// NVFP4 block-scaled batched GEMV and small-N GEMM on the tensor cores
+// (tcgen05, sm_103a), pre-permuted scales only.
 //
 // The hardware block-scaled MMA (kind::mxf4nvf4, 16-element blocks with E4M3
 // scales, scale_vec::4X) computes, for a 128-row tile of A and an N = 16 row
 // operand B, D[m][n] += sum_k E2M1(a[m][k]) * sfa[m][k/16] * E2M1(b[n][k]) *
 // sfb[n][k/16] over K = 64 per instruction, accumulating in fp32 in tensor
-// memory (TMEM).  The GEMV puts b in row 0 of B (rows 1..15 are zeros) and
-// keeps column 0 of D.  The 128x4 scale atom of the pre-permuted layout is
-// byte for byte the source the 32x128b.warpx4 TMEM copy expects, so one atom
-// (512 B) feeds one MMA's scales with no repacking.
+// memory (TMEM).  Rows 0..N-1 of B hold the N <= 16 vectors (one for the
+// GEMV), the other rows are zeros, and the epilogue reads columns 0..N-1 of
+// D.  The 128x4 scale atom of the pre-permuted layout is byte for byte the
+// source of one 32x128b.warpx4 TMEM copy, so the scales need no repacking:
+// one sfa atom and one sfb atom (512 B each) feed one MMA.  (An MMA's scale
+// address in TMEM is a 4-column-aligned copy destination.)
 //
 // One CTA (192 threads):
-//   warp 0      one lane issues the copies of each stage: A as a 128-row x
-//               128-byte TMA tile (128-byte swizzle), b's 128-byte chunk as a
-//               1-row TMA tile, and the stage's 4 sfa atoms and 4 sfb atoms as
-//               two 2 KB bulk copies (consecutive atoms are adjacent in memory);
-//   warp 1      allocates TMEM; one lane copies each stage's scale atoms into
-//               TMEM (tcgen05.cp) and issues the stage's 4 MMAs, then commits
-//               the stage back to the producer and, at the end of a tile, the
-//               accumulator to the epilogue;
+//   warp 0      one lane issues the copies of each 256-element K stage: A as
+//               a 128-row x 128-byte TMA tile (128-byte swizzle), b as an
+//               N-row TMA tile, and the stage's 4 sfa atoms and 4 sfb atoms as
+//               two 2 KB bulk copies (consecutive atoms are adjacent);
+//   warp 1      allocates TMEM; one lane copies the stage's 8 atoms into TMEM
+//               (tcgen05.cp) and issues its MMAs, then
+//               commits the stage back to the producer and, at the end of a
+//               tile, the (double-buffered) accumulator to the epilogue;
 //   warps 2..5  read the accumulator (one TMEM lane quarter each), and either
-//               store c or send the partial sums to the cluster's rank 0.
+//               store c or hand their partial sums to the cluster's rank 0.
+// The copies and MMAs of one stage complete one after another; a CTA has 2 or
+// 4 stages and several CTAs share an SM, whose independent chains overlap.
 // Split K: the KS CTAs of a cluster share every tile, each taking a
 // contiguous range of 256-element K stages (the rank that takes an extra
-// stage rotates from tile to tile); ranks 1..KS-1 store their partial sums
-// into rank 0's shared memory (distributed shared memory) and rank 0 adds
-// them in rank order, so the result does not depend on timing.
+// stage rotates from tile to tile); ranks 1..KS-1 leave their partial sums
+// in their own shared memory and rank 0 reads them (distributed shared
+// memory) and adds them in rank order, so the result does not depend on
+// timing or on the grid.
 // Clusters are persistent: cluster i takes tiles i, i + clusters, ...
 //
 // Every wait on an mbarrier gives up after kWaitNs of global time, counts a
@@ -50,21 +55,27 @@ __device__ int g_tc_timeouts;
 namespace {
 
 constexpr int kTcThreads = 192;
-constexpr int kTcStages = 6;
-constexpr int kTcMaxCluster = 8;
 constexpr uint32_t kTcABytes = 128 * 128;   // 128 rows x 256 elements
-constexpr uint32_t kTcBBytes = 16 * 128;    // 16 rows x 256 elements (row 0 = b)
+constexpr uint32_t kTcBBytes = 16 * 128;    // 16 rows x 256 elements (rows 0..N-1 = b)
 constexpr uint32_t kTcSfBytes = 4 * 512;    // 4 scale atoms (K = 256)
-constexpr uint32_t kTcStageBytes = kTcABytes + kTcBBytes + 2 * kTcSfBytes;
-constexpr uint32_t kTcRedBytes = 2 * kTcMaxCluster * 128 * 4;
-constexpr uint32_t kTcSmemBytes = kTcStages * kTcStageBytes + kTcRedBytes + 1024;
-constexpr uint32_t kTmemCols = 256;
-// TMEM columns: accumulators [2][16] at 0, sfa [stage][4 atoms][4 cols] at 32,
-// sfb likewise after them
-constexpr uint32_t kTmemSfa = 32;
-constexpr uint32_t kTmemSfb = kTmemSfa + kTcStages * 16;
-static_assert(kTmemSfb + kTcStages * 16 <= kTmemCols, "TMEM columns");
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s
+
+// TMEM columns a CTA allocates: accumulators [2][16], then sfa and sfb
+// [stage][4 atoms][4 columns] each (a power of two, at least 32).
+__host__ __device__ constexpr uint32_t tc_tmem_cols(int stages) { return stages <= 2 ? 128u : 256u; }
+constexpr uint32_t tc_smem_bytes(int stages, int nc) {
+  return (uint32_t)stages * (kTcABytes + kTcBBytes + 2 * kTcSfBytes) +
+         2u * (uint32_t)nc * 128u * 4u + 1024u;
+}
+static_assert(32 + 32 * 2 <= tc_tmem_cols(2) && 32 + 32 * 4 <= tc_tmem_cols(4), "TMEM columns");
+// The SM's 512 TMEM columns are never oversubscribed, so an allocation never
+// waits for another CTA: shared memory (228 KB per SM, 1 KB of it reserved
+// per CTA) admits at most 4 CTAs of 2 stages (128 columns), at most 2 of 4
+// stages (256), and 2-stage CTAs beside a 4-stage one at most 2.
+static_assert(5 * (tc_smem_bytes(2, 1) + 1024) > 228 * 1024, "at most 4 CTAs of 2 stages");
+static_assert(3 * (tc_smem_bytes(4, 1) + 1024) > 228 * 1024, "at most 2 CTAs of 4 stages");
+static_assert((tc_smem_bytes(4, 1) + 1024) + 3 * (tc_smem_bytes(2, 1) + 1024) > 228 * 1024,
+              "at most 2 CTAs of 2 stages beside one of 4");
 
 // Instruction descriptor of the block-scaled MMA: A and B E2M1 (format 1),
 // both K-major, N = 16 (N/8 at bit 17), UE4M3 scales (bit 23 clear),
@@ -73,15 +84,15 @@ constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u
 
 struct TcParams {
   CUtensorMap tmap_a;  // uint8 {K/2, M, L}, box {128, 128, 1}, 128-byte swizzle
-  CUtensorMap tmap_b;  // uint8 {K/2, L}, box {128, 1}, 128-byte swizzle
+  CUtensorMap tmap_b;  // uint8 {K/2, N, L}, box {128, N, 1}, 128-byte swizzle
   const uint8_t* sfa;  // permuted [L][rest_m][rest_k][512]
-  const uint8_t* sfb;  // permuted, one 128-row block per batch: [L][rest_k][512] (stride below)
-  uint16_t* c;
-  const uint16_t* bias;
+  const uint8_t* sfb;  // permuted, one 128-row block per batch (rows 0..N-1): [L][rest_k][512]
+  uint16_t* c;         // fp16 [L][N][M]
+  const uint16_t* bias;  // fp16 [L][N][M], or null
   float alpha;
   int64_t M;
-  int64_t sfb_stride;
-  int32_t rest_m, rest_k, kstages, tiles;
+  int64_t sfb_stride;  // bytes from batch l to l+1 of sfb
+  int32_t N, rest_m, rest_k, kstages, tiles;
 };
 
 // fp32 -> fp16 output with the optional scale and bias: the same formula as
@@ -160,8 +171,10 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
-__device__ __forceinline__ void st_remote_f32(uint32_t cluster_addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+__device__ __forceinline__ float ld_remote_f32(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+  return v;
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
@@ -184,14 +197,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
       "[%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
-      "[%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
@@ -243,6 +248,41 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdes
       "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"((uint32_t)accumulate), "r"(sfa), "r"(sfb)
       : "memory");
 }
+// Columns 0..NC-1 of this warp's 32 TMEM lanes (lane i of the warp gets
+// row 32*quarter + i), as fp32.
+template <int NC>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&out)[NC]) {
+  uint32_t v[NC];
+  if constexpr (NC == 1) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v[0]) : "r"(taddr));
+  } else if constexpr (NC == 2) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
+                 : "=r"(v[0]), "=r"(v[1])
+                 : "r"(taddr));
+  } else if constexpr (NC == 4) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "r"(taddr));
+  } else if constexpr (NC == 8) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                   "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr));
+  } else {
+    static_assert(NC == 16, "NC in {1, 2, 4, 8, 16}");
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+  }
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int n = 0; n < NC; ++n) out[n] = __uint_as_float(v[n]);
+}
+
 // Arrive on the mbarrier once every tcgen05 operation this thread issued so
 // far has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -251,9 +291,12 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
+// S: pipeline stages per CTA (2 or 4; fewer stages let more CTAs share an SM,
+// whose independent copy+MMA chains then overlap).  NC: accumulator columns
+// read back (a power of two >= N, the rows of B that hold data).
+template <int S, int NC>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    nvfp4_gemv_tc_kernel(const __grid_constant__ TcParams p) {
-  constexpr int S = kTcStages;
+    nvfp4_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t tc_smem[];
   __shared__ __align__(8) uint64_t bars[2 * S + 9];
   __shared__ uint32_t tmem_slot;
@@ -264,8 +307,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t b_s = a_s + S * kTcABytes;
   const uint32_t sfa_s = b_s + S * kTcBBytes;
   const uint32_t sfb_s = sfa_s + S * kTcSfBytes;
-  const uint32_t red_s = sfb_s + S * kTcSfBytes;
-  const float* red = reinterpret_cast<const float*>(tc_smem + (red_s - raw));
+  const uint32_t red_s = sfb_s + S * kTcSfBytes;  // this CTA's partial sums [2][NC][128]
+  uint8_t* const gen = tc_smem - raw;            // generic pointer = gen + shared address
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int st) { return bar0 + 8u * st; };
   auto empty_bar = [&](int st) { return bar0 + 8u * (S + st); };
@@ -274,6 +317,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t rfull_bar = bar0 + 8u * (2 * S + 4);   // [2] (rank 0)
   const uint32_t rfree_bar = bar0 + 8u * (2 * S + 6);   // [2] (ranks > 0)
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 8);
+  // TMEM columns: accumulators [2][16], sfa and sfb [stage][4 atoms][4]
+  constexpr uint32_t kSfaCol = 32, kSfbCol = 32 + 16 * S, kTmemCols = tc_tmem_cols(S);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ks = cluster_size(), rank = cluster_rank();
@@ -295,11 +340,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(drain_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // rows 1..15 of every B stage stay zero (the b copy writes row 0 only)
-  for (uint32_t i = threadIdx.x; i < S * kTcBBytes / 16; i += kTcThreads) {
-    if ((i % (kTcBBytes / 16)) >= 128 / 16)
-      *reinterpret_cast<uint4*>(tc_smem + (b_s - raw) + 16 * i) = make_uint4(0, 0, 0, 0);
-  }
+  // rows N..15 of every B stage start as zeros and are never written again
+  // (the b copy fills rows 0..N-1 only)
+  for (uint32_t i = threadIdx.x; i < S * kTcBBytes / 16; i += kTcThreads)
+    if ((int)((i % (kTcBBytes / 16)) / 8) >= p.N)
+      *reinterpret_cast<uint4*>(gen + b_s + 16 * i) = make_uint4(0, 0, 0, 0);
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -315,10 +360,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = tmem_slot;
   bool ok = true;
 
-  // The contiguous K-stage range of this rank for the cluster's j-th tile.
-  auto stage_range = [&](int j, int& s0, int& cnt) {
+  // The contiguous K-stage range of this rank for tile t (the rank that takes
+  // an extra stage rotates with t, so the split, and the rounding, depend on
+  // the tile and the cluster size only, not on the grid).
+  auto stage_range = [&](int t, int& s0, int& cnt) {
     const int per = p.kstages / (int)ks, extra = p.kstages % (int)ks;
-    const int rr = (int)((rank + (uint32_t)j) % ks);
+    const int rr = (int)((rank + (uint32_t)t) % ks);
     cnt = per + (rr < extra ? 1 : 0);
     s0 = rr * per + (rr < extra ? rr : extra);
   };
@@ -328,9 +375,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       if (ntiles > 0) {  // the first stages' A lines, ahead of the dependency wait
         int s0, cnt;
-        stage_range(0, s0, cnt);
+        stage_range(cid, s0, cnt);
         const int l = cid / p.rest_m, mt = cid % p.rest_m;
-        for (int i = 0; i < cnt && i < S; ++i) tma_prefetch_3d(&p.tmap_a, (s0 + i) * 128, mt * 128, l);
+        for (int i = 0; i < cnt && i < 2 * S; ++i)
+          tma_prefetch_3d(&p.tmap_a, (s0 + i) * 128, mt * 128, l);
       }
       pdl_wait();
       int st = 0;
@@ -339,15 +387,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int t = cid + j * nclusters;
         const int l = t / p.rest_m, mt = t % p.rest_m;
         int s0, cnt;
-        stage_range(j, s0, cnt);
+        stage_range(t, s0, cnt);
         for (int i = 0; i < cnt; ++i) {
           const int s = s0 + i;
           const int nk = min(4, p.rest_k - 4 * s);
           if (mbar_wait<false>(empty_bar(st), ph ^ 1u, ok)) {
             const uint32_t fb = full_bar(st);
-            mbar_expect_tx(fb, kTcABytes + 128u + 2u * (uint32_t)nk * 512u);
+            mbar_expect_tx(fb, kTcABytes + 128u * (uint32_t)p.N + 2u * (uint32_t)nk * 512u);
             tma_load_3d(a_s + st * kTcABytes, &p.tmap_a, s * 128, mt * 128, l, fb);
-            tma_load_2d(b_s + st * kTcBBytes, &p.tmap_b, s * 128, l, fb);
+            tma_load_3d(b_s + st * kTcBBytes, &p.tmap_b, s * 128, 0, l, fb);
             bulk_load(sfa_s + st * kTcSfBytes,
                       p.sfa + (((int64_t)l * p.rest_m + mt) * p.rest_k + 4 * s) * 512,
                       (uint32_t)nk * 512u, fb);
@@ -373,41 +421,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     pdl_wait();
-    if (lane == 0) {
-      int st = 0;
-      uint32_t ph = 0;
-      for (int j = 0; j < ntiles; ++j) {
-        const int acc = j & 1;
-        const uint32_t d = tmem + (uint32_t)(16 * acc);
-        mbar_wait<false>(dempty_bar + 8u * acc, ((uint32_t)(j >> 1) & 1u) ^ 1u, ok);
-        tc_fence_after();
-        int s0, cnt;
-        stage_range(j, s0, cnt);
-        for (int i = 0; i < cnt; ++i) {
-          const int s = s0 + i;
-          const int nk = min(4, p.rest_k - 4 * s);
-          if (mbar_wait<false>(full_bar(st), ph, ok)) {
-            tc_fence_after();
-            for (int kk = 0; kk < nk; ++kk) {
-              tc_copy_atom(tmem + kTmemSfa + (uint32_t)(16 * st + 4 * kk),
-                           desc_atom(sfa_s + st * kTcSfBytes + 512u * kk));
-              tc_copy_atom(tmem + kTmemSfb + (uint32_t)(16 * st + 4 * kk),
-                           desc_atom(sfb_s + st * kTcSfBytes + 512u * kk));
-            }
-            for (int kk = 0; kk < nk; ++kk)
-              tc_mma(d, desc_sw128(a_s + st * kTcABytes + 32u * kk),
-                     desc_sw128(b_s + st * kTcBBytes + 32u * kk),
-                     tmem + kTmemSfa + (uint32_t)(16 * st + 4 * kk),
-                     tmem + kTmemSfb + (uint32_t)(16 * st + 4 * kk), i > 0 || kk > 0);
-            tc_commit(empty_bar(st));
+    int st = 0;
+    uint32_t ph = 0;
+    for (int j = 0; j < ntiles; ++j) {
+      const int acc = j & 1;
+      const uint32_t d = tmem + (uint32_t)(16 * acc);
+      if (lane == 0) mbar_wait<false>(dempty_bar + 8u * acc, ((uint32_t)(j >> 1) & 1u) ^ 1u, ok);
+      int s0, cnt;
+      stage_range(cid + j * nclusters, s0, cnt);
+      for (int i = 0; i < cnt; ++i) {
+        const int s = s0 + i;
+        const int nk = min(4, p.rest_k - 4 * s);
+        if (lane == 0 && mbar_wait<false>(full_bar(st), ph, ok)) {
+          tc_fence_after();
+          for (int kk = 0; kk < nk; ++kk) {
+            tc_copy_atom(tmem + kSfaCol + (uint32_t)(16 * st + 4 * kk),
+                         desc_atom(sfa_s + st * kTcSfBytes + 512u * kk));
+            tc_copy_atom(tmem + kSfbCol + (uint32_t)(16 * st + 4 * kk),
+                         desc_atom(sfb_s + st * kTcSfBytes + 512u * kk));
           }
-          if (++st == S) {
-            st = 0;
-            ph ^= 1u;
-          }
+          for (int kk = 0; kk < nk; ++kk)
+            tc_mma(d, desc_sw128(a_s + st * kTcABytes + 32u * kk),
+                   desc_sw128(b_s + st * kTcBBytes + 32u * kk),
+                   tmem + kSfaCol + (uint32_t)(16 * st + 4 * kk),
+                   tmem + kSfbCol + (uint32_t)(16 * st + 4 * kk), i > 0 || kk > 0);
+          tc_commit(empty_bar(st));
         }
-        if (ok) tc_commit(dfull_bar + 8u * acc);
+        if (++st == S) {
+          st = 0;
+          ph ^= 1u;
+        }
       }
+      if (lane == 0 && ok) tc_commit(dfull_bar + 8u * acc);
+    }
+    if (lane == 0) {
       // every MMA and TMEM copy has finished before TMEM is released
       tc_commit(drain_bar);
       bool drain_ok = true;
@@ -418,42 +465,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_wait();
     const uint32_t q = (uint32_t)(warp & 3);  // the TMEM lane quarter this warp may read
     const int r = (int)(32 * q) + lane;       // row inside the tile
+    float* const red = reinterpret_cast<float*>(gen + red_s);
     for (int j = 0; j < ntiles; ++j) {
       const int t = cid + j * nclusters;
       const int l = t / p.rest_m, mt = t % p.rest_m;
       const int acc = j & 1;
       mbar_wait<false>(dfull_bar + 8u * acc, (uint32_t)(j >> 1) & 1u, ok);
       ok = __all_sync(0xffffffffu, ok);  // the TMEM load below is warp-collective
-      float part = 0.f;
-      if (ok) {
+      float part[NC];
+#pragma unroll
+      for (int n = 0; n < NC; ++n) part[n] = 0.f;
+      if (ok && p.kstages > 0) {  // K = 0: the sums are zero and no MMA ran
         tc_fence_after();
-        uint32_t v;
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
-                     : "=r"(v)
-                     : "r"(tmem + (uint32_t)(16 * acc) + ((32u * q) << 16)));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        part = __uint_as_float(v);
+        tmem_load_cols<NC>(tmem + (uint32_t)(16 * acc) + ((32u * q) << 16), part);
       }
       tc_fence_before();
       mbar_arrive(dempty_bar + 8u * acc);
       const int64_t m = (int64_t)mt * 128 + r;
       const int buf = j & 1;
       const uint32_t use = (uint32_t)(j >> 1);
-      if (ks == 1) {
-        if (ok && m < p.M) p.c[(int64_t)l * p.M + m] = finish_output_tc(p.alpha, p.bias, part, (int64_t)l * p.M + m);
-      } else if (rank != 0) {
-        // wait until rank 0 has read this buffer's previous use, then send
+      if (ks > 1 && rank != 0) {
+        // wait until rank 0 has read this buffer's previous use, then publish
         mbar_wait<true>(rfree_bar + 8u * buf, (use & 1u) ^ 1u, ok);
-        const uint32_t slot = red_s + 4u * (uint32_t)((buf * kTcMaxCluster + (int)rank) * 128 + r);
-        st_remote_f32(map_rank(slot, 0), part);
+#pragma unroll
+        for (int n = 0; n < NC; ++n) red[(buf * NC + n) * 128 + r] = part[n];
         mbar_arrive_remote(map_rank(rfull_bar + 8u * buf, 0));
-      } else {
-        float sum = part;
-        if (mbar_wait<true>(rfull_bar + 8u * buf, use & 1u, ok)) {
-          for (uint32_t k = 1; k < ks; ++k) sum += red[(buf * kTcMaxCluster + (int)k) * 128 + r];
+        continue;
+      }
+      if (ks > 1) {
+        const bool got = mbar_wait<true>(rfull_bar + 8u * buf, use & 1u, ok);
+        for (uint32_t k = 1; k < ks; ++k) {
+#pragma unroll
+          for (int n = 0; n < NC; ++n)
+            if (got) part[n] += ld_remote_f32(map_rank(red_s + 4u * (uint32_t)((buf * NC + n) * 128 + r), k));
         }
         for (uint32_t k = 1; k < ks; ++k) mbar_arrive_remote(map_rank(rfree_bar + 8u * buf, k));
-        if (ok && m < p.M) p.c[(int64_t)l * p.M + m] = finish_output_tc(p.alpha, p.bias, sum, (int64_t)l * p.M + m);
+      }
+      if (ok && m < p.M) {
+#pragma unroll
+        for (int n = 0; n < NC; ++n) {
+          if (n < p.N) {
+            const int64_t idx = ((int64_t)l * p.N + n) * p.M + m;
+            p.c[idx] = finish_output_tc(p.alpha, p.bias, part[n], idx);
+          }
+        }
       }
     }
   }
@@ -484,15 +539,30 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-cudaError_t tc_launch_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], int ks,
-                             int64_t ctas, cudaStream_t stream) {
-  cudaError_t err = cudaFuncSetAttribute(nvfp4_gemv_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
+using TcKernel = void (*)(TcParams);
+
+// The kernel instance for (stages, columns read back); null if none.
+TcKernel tc_kernel_for(int stages, int nc) {
+#define NVFP4_TC(S_, NC_) \
+  if (stages == S_ && nc == NC_) return nvfp4_tc_kernel<S_, NC_>;
+  NVFP4_TC(2, 1) NVFP4_TC(2, 2) NVFP4_TC(2, 4) NVFP4_TC(2, 8) NVFP4_TC(2, 16)
+  NVFP4_TC(4, 1) NVFP4_TC(4, 2) NVFP4_TC(4, 4) NVFP4_TC(4, 8) NVFP4_TC(4, 16)
+#undef NVFP4_TC
+  return nullptr;
+}
+
+int tc_columns(int64_t n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : n <= 8 ? 8 : 16; }
+
+cudaError_t tc_launch_config(TcKernel kern, int stages, int nc, cudaLaunchConfig_t& cfg,
+                             cudaLaunchAttribute (&attr)[2], int ks, int64_t ctas,
+                             cudaStream_t stream) {
+  const uint32_t smem = tc_smem_bytes(stages, nc);
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   cfg = {};
   cfg.gridDim = dim3((unsigned)ctas, 1, 1);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
-  cfg.dynamicSmemBytes = kTcSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)ks;
@@ -507,14 +577,17 @@ cudaError_t tc_launch_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr
 
 }  // namespace
 
-cudaError_t launch_gemv_tc(const GemvParams& gp, int64_t L, int ks, int64_t ctas,
-                           cudaStream_t stream) {
+cudaError_t launch_gemv_tc(const GemvParams& gp, int64_t N, int64_t L, int64_t b_row_stride,
+                           int stages, int ks, int64_t ctas, cudaStream_t stream) {
+  const int nc = tc_columns(N);
+  TcKernel kern = tc_kernel_for(stages, nc);
+  if (kern == nullptr || N < 1 || N > 16) return cudaErrorInvalidValue;
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-  if (encode == nullptr) return cudaErrorNotSupported;
+  if (encode == nullptr && gp.half_k > 0) return cudaErrorNotSupported;
   TcParams p;
   memset(&p, 0, sizeof(p));
   const cuuint64_t half_k = (cuuint64_t)gp.half_k;
-  {
+  if (half_k > 0) {  // K = 0 reads nothing
     const cuuint64_t dims[3] = {half_k, (cuuint64_t)gp.M, (cuuint64_t)L};
     const cuuint64_t strides[2] = {half_k, half_k * (cuuint64_t)gp.M};
     const cuuint32_t box[3] = {128, 128, 1};
@@ -524,12 +597,12 @@ cudaError_t launch_gemv_tc(const GemvParams& gp, int64_t L, int ks, int64_t ctas
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  {
-    const cuuint64_t dims[2] = {half_k, (cuuint64_t)L};
-    const cuuint64_t strides[1] = {(cuuint64_t)gp.b_stride};
-    const cuuint32_t box[2] = {128, 1};
-    const cuuint32_t estr[2] = {1, 1};
-    if (encode(&p.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(gp.b), dims,
+  if (half_k > 0) {
+    const cuuint64_t dims[3] = {half_k, (cuuint64_t)N, (cuuint64_t)L};
+    const cuuint64_t strides[2] = {(cuuint64_t)b_row_stride, (cuuint64_t)gp.b_stride};
+    const cuuint32_t box[3] = {128, (cuuint32_t)N, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&p.tmap_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(gp.b), dims,
                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -541,24 +614,28 @@ cudaError_t launch_gemv_tc(const GemvParams& gp, int64_t L, int ks, int64_t ctas
   p.alpha = gp.alpha;
   p.M = gp.M;
   p.sfb_stride = gp.sfb_stride;
+  p.N = (int32_t)N;
   p.rest_m = gp.rest_m;
   p.rest_k = gp.rest_k;
   p.kstages = (gp.rest_k + 3) / 4;
   p.tiles = (int32_t)(L * gp.rest_m);
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  cudaError_t err = tc_launch_config(cfg, attr, ks, ctas, stream);
+  cudaError_t err = tc_launch_config(kern, stages, nc, cfg, attr, ks, ctas, stream);
   if (err != cudaSuccess) return err;
-  return cudaLaunchKernelEx(&cfg, nvfp4_gemv_tc_kernel, p);
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-cudaError_t tc_max_active_clusters(int ks, int* out) {
+cudaError_t tc_max_active_clusters(int stages, int64_t N, int ks, int* out) {
+  const int nc = tc_columns(N);
+  TcKernel kern = tc_kernel_for(stages, nc);
+  if (kern == nullptr) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  cudaError_t err = tc_launch_config(cfg, attr, ks, ks, nullptr);
+  cudaError_t err = tc_launch_config(kern, stages, nc, cfg, attr, ks, ks, nullptr);
   if (err != cudaSuccess) return err;
   cfg.numAttrs = 1;  // the cluster shape alone
-  return cudaOccupancyMaxActiveClusters(out, nvfp4_gemv_tc_kernel, &cfg);
+  return cudaOccupancyMaxActiveClusters(out, kern, &cfg);
 }
 
 cudaError_t tc_wait_timeouts(int reset, int* out) {

@@ -77,6 +77,21 @@ def make_problem(M: int, K: int, L: int, seed: int = 0) -> dict:
     }
 
 
+def make_gemm_problem(M: int, N: int, K: int, L: int, seed: int = 0) -> dict:
+    """Plain-layout inputs of a small-N GEMM: the GEMV recipe with b and sfb
+    drawn as N rows per batch (b [L, N, K//2], sfb [L, N, K//16]); N = 1 gives
+    make_problem's bytes."""
+    if K % 64 != 0:
+        raise ValueError("K must be a multiple of 64")
+    base = seed * 16
+    return {
+        "a": random_bytes(base + STREAM_A, L * M * (K // 2)).reshape(L, M, K // 2),
+        "b": random_bytes(base + STREAM_B, L * N * (K // 2)).reshape(L, N, K // 2),
+        "sfa": scale_bytes(base + STREAM_SFA, L * M * (K // 16)).reshape(L, M, K // 16),
+        "sfb": scale_bytes(base + STREAM_SFB, L * N * (K // 16)).reshape(L, N, K // 16),
+    }
+
+
 # The benchmark workloads: (name, M, K, L).  The first is a small parity case,
 # the next three are the shapes the submissions time (submission 69953's
 # docstring performance targets), the last a 1.2 GB sustained-bandwidth case.
@@ -92,3 +107,18 @@ WORKLOADS = [
 def algorithmic_bytes(M: int, K: int, L: int) -> int:
     """Bytes one call must move at least: A + sfa + b + sfb + c."""
     return L * M * (K // 2 + K // 16 + 2) + L * (K // 2 + K // 16)
+
+
+# Small-N GEMM workloads (decode batches of N vectors on the GEMV shapes):
+# (name, M, N, K, L).
+GEMM_WORKLOADS = [
+    ("M7168_N8_K2048_L4", 7168, 8, 2048, 4),
+    ("M4096_N4_K7168_L8", 4096, 4, 7168, 8),
+    ("M7168_N16_K16384_L1", 7168, 16, 16384, 1),
+    ("M16384_N8_K8192_L16", 16384, 8, 8192, 16),
+]
+
+
+def gemm_algorithmic_bytes(M: int, N: int, K: int, L: int) -> int:
+    """Bytes a small-N GEMM must move: A + sfa + N x (b + sfb) read, c written."""
+    return L * (M * (K // 2 + K // 16) + N * (K // 2 + K // 16) + 2 * N * M)

@@ -149,6 +149,33 @@ def gemv_ex(a, b, sfa, sfb, M: int, K: int, L: int, alpha: float = 1.0, bias=Non
     return fp16_rne(y), y, abs(float(alpha)) * sabs
 
 
+def gemm_small_n(a, b, sfa, sfb, M: int, N: int, K: int, L: int, alpha: float = 1.0,
+                 bias=None):
+    """Small-N GEMM: N dot products per row of A, one per vector of b::
+
+        c[l, n, m] = fp16(alpha * sum_k E2M1(a[m,k,l]) * E4M3(sfa[m,k//16,l])
+                                      * E2M1(b[n,k,l]) * E4M3(sfb[n,k//16,l]) + bias[l, n, m])
+
+    i.e. the GEMV definition above applied to each vector n (the pages' harness
+    multiplies A by an N-column B through ``torch._scaled_mm``, submission
+    103289's ``cute_jit_kernel`` padding N to 128).  ``b`` uint8 [L, N, K//2],
+    ``sfb`` uint8 [L, N, K//16], ``bias`` fp16 bits [L, N, M] or None.
+    Returns ``(c_bits [L, N, M], values, |alpha| * sumabs)`` as :func:`gemv_ex`.
+    """
+    b_ = np.ascontiguousarray(np.asarray(b, dtype=np.uint8).reshape(L, N, K // 2))
+    sb_ = np.ascontiguousarray(np.asarray(sfb, dtype=np.uint8).reshape(L, N, K // 16))
+    bias_ = None if bias is None else np.asarray(bias, dtype=np.uint16).reshape(L, N, M)
+    c = np.zeros((L, N, M), dtype=np.uint16)
+    vals = np.zeros((L, N, M), dtype=np.float64)
+    tol = np.zeros((L, N, M), dtype=np.float64)
+    for n in range(N):
+        bn = None if bias_ is None else np.ascontiguousarray(bias_[:, n, :])
+        c[:, n, :], vals[:, n, :], tol[:, n, :] = gemv_ex(
+            a, np.ascontiguousarray(b_[:, n, :]), sfa, np.ascontiguousarray(sb_[:, n, :]),
+            M, K, L, alpha, bn)
+    return c, vals, tol
+
+
 def gemv_at(a, b, sfa, sfb, M: int, K: int, L: int, m_idx, l_idx):
     """fp64 path for the selected outputs ``(m_idx[i], l_idx[i])`` only."""
     _check_shape(M, K, L)

@@ -4,6 +4,7 @@ The library loads and exports every function the header declares; argument
 validation rejects bad calls before touching the GPU; the launch planner
 and the kernel's row partition are checked as host arithmetic.
 """
+import ctypes
 import os
 import re
 import subprocess
@@ -376,3 +377,39 @@ def test_pipelined_tasks_cover_every_row_once(M, L, ctas, ks, ri, perm, groups):
                                 seen.append((l, m))
                 r += cnt
     assert sorted(seen) == [(l, m) for l in range(L) for m in range(M)]
+
+
+def test_gemm_small_n_validation(lib):
+    G = lib.nvfp4_gemm_small_n
+    E = lib.nvfp4_gemm_small_n_explicit
+    ptrs = (64, 64, 64, 64, 64)
+    # (M, N, K, L): checked before any CUDA call
+    assert G(*ptrs, 300, 17, 1024, 2, None, None) == nv.ERR_UNSUPPORTED_SHAPE
+    assert G(*ptrs, 300, -1, 1024, 2, None, None) == nv.ERR_INVALID_VALUE
+    assert G(*ptrs, 300, 4, 1000, 2, None, None) == nv.ERR_UNSUPPORTED_SHAPE
+    assert G(*ptrs, 0, 4, 1024, 2, None, None) == nv.OK
+    assert G(*ptrs, 300, 0, 1024, 2, None, None) == nv.OK
+    assert G(*ptrs, 300, 4, 1024, 0, None, None) == nv.OK
+    assert G(None, 64, 64, 64, 64, 300, 4, 1024, 2, None, None) == nv.ERR_INVALID_VALUE
+    assert G(64, 64, 64, 64, None, 300, 4, 1024, 2, None, None) == nv.ERR_INVALID_VALUE
+    assert G(64, 80, 64, 64, 64, 300, 4, 1024, 2, None, None) == nv.ERR_MISALIGNED
+    assert G(64, 64, 64, 64, 65, 300, 4, 1024, 2, None, None) == nv.ERR_MISALIGNED
+    # b batch stride below N*K/2, or not a multiple of 32
+    opt = nv._Options(1.0, None, 4 * 512 - 32, 0)
+    assert G(*ptrs, 300, 4, 1024, 2, ctypes.byref(opt), None) == nv.ERR_INVALID_VALUE
+    opt = nv._Options(1.0, None, 4 * 512 + 16, 0)
+    assert G(*ptrs, 300, 4, 1024, 2, ctypes.byref(opt), None) == nv.ERR_MISALIGNED
+    # sfb batch stride below (K/64)*512, or not a multiple of 16
+    opt = nv._Options(1.0, None, 0, 16 * 512 - 16)
+    assert G(*ptrs, 300, 4, 1024, 2, ctypes.byref(opt), None) == nv.ERR_INVALID_VALUE
+    opt = nv._Options(1.0, None, 0, 16 * 512 + 8)
+    assert G(*ptrs, 300, 4, 1024, 2, ctypes.byref(opt), None) == nv.ERR_MISALIGNED
+    # explicit schedules: stages 2 or 4; cluster sizes 1/2/4/8 within the K stages; whole clusters
+    args = ptrs + (300, 4, 1024, 2)
+    assert E(*args, 3, 1, 1, None) == nv.ERR_INVALID_VALUE
+    assert E(*args, 2, 3, 3, None) == nv.ERR_INVALID_VALUE
+    assert E(*args, 2, 8, 8, None) == nv.ERR_INVALID_VALUE  # K = 1024: 4 stages
+    assert E(*args, 4, 2, 3, None) == nv.ERR_INVALID_VALUE
+    assert E(*args, 2, 1, 0, None) == nv.ERR_INVALID_VALUE
+    assert E(*(ptrs + (300, 4, 0, 2)), 2, 2, 2, None) == nv.ERR_INVALID_VALUE  # K = 0: no split
+    assert E(*(ptrs + (0, 4, 1024, 2)), 2, 1, 1, None) == nv.OK

@@ -35,8 +35,9 @@ def to_dev(x):
     return torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
 
 
-def run_tc(a, b, sfa_plain, sfb_plain, M, K, L, ks, ctas):
-    """One tensor-core launch on oracle-repacked scales; returns c's fp16 bits [L, M]."""
+def run_tc(a, b, sfa_plain, sfb_plain, M, K, L, ks, ctas, stages=4):
+    """One tensor-core launch (stages per CTA, clusters of ks) on oracle-repacked
+    scales; returns c's fp16 bits [L, M]."""
     sfa = to_dev(oracle.repack_scales(sfa_plain, M, K, L))
     sfb = to_dev(oracle.repack_scales(np.asarray(sfb_plain).reshape(L, 1, K // 16), 1, K, L))
     ad, bd = to_dev(a), to_dev(b)
@@ -44,7 +45,7 @@ def run_tc(a, b, sfa_plain, sfb_plain, M, K, L, ks, ctas):
     buf = torch.full((L * M + 2 * pad,), SENTINEL, dtype=torch.float16, device=DEV)
     c = buf[pad:pad + L * M]
     nv.nvfp4_gemv_explicit(ad.data_ptr(), bd.data_ptr(), sfa.data_ptr(), sfb.data_ptr(),
-                           c.data_ptr(), M, K, L, nv.SF_PERMUTED_128x4, nv.KERNEL_TENSOR, 4, ks,
+                           c.data_ptr(), M, K, L, nv.SF_PERMUTED_128x4, nv.KERNEL_TENSOR, stages, ks,
                            ctas, torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert nv.nvfp4_tensor_wait_timeouts(reset=True) == 0, "a pipeline wait ran out"
@@ -54,9 +55,9 @@ def run_tc(a, b, sfa_plain, sfb_plain, M, K, L, ks, ctas):
     return whole[pad:pad + L * M].reshape(L, M)
 
 
-def check(p, M, K, L, ks, ctas):
+def check(p, M, K, L, ks, ctas, stages=4):
     ref, sums, sumabs = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
-    got = run_tc(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L, ks, ctas)
+    got = run_tc(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L, ks, ctas, stages)
     parity.assert_parity(got, ref, sums, sumabs, f"tensor M={M} K={K} L={L} ks={ks} ctas={ctas}")
     return got
 
@@ -93,10 +94,11 @@ TC_CASES = [
 ]
 
 
+@pytest.mark.parametrize("stages", [2, 4])
 @pytest.mark.parametrize("M,K,L,ks,ctas", TC_CASES)
-def test_parity_tensor_kernel(M, K, L, ks, ctas):
+def test_parity_tensor_kernel(M, K, L, ks, ctas, stages):
     p = synthetic.make_problem(M, K, L, seed=M + K + ks)
-    check(p, M, K, L, ks, ctas)
+    check(p, M, K, L, ks, ctas, stages)
 
 
 def test_tensor_kernel_is_deterministic():
@@ -105,10 +107,16 @@ def test_tensor_kernel_is_deterministic():
     first = check(p, M, K, L, 4, 8)
     again = run_tc(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L, 4, 8)
     assert np.array_equal(first, again)
+    # the rounding depends on the cluster size only: other grids and stage counts agree
+    for ctas, stages in ((4, 2), (32, 4), (64, 2)):
+        assert np.array_equal(first, run_tc(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L, 4,
+                                            ctas, stages))
 
 
-@pytest.mark.parametrize("name,ks,ctas", [("M7168_K2048_L4", 2, 152), ("M7168_K16384_L1", 8, 152)])
-def test_tensor_kernel_full_size(name, ks, ctas):
+@pytest.mark.parametrize("name,ks,ctas,stages", [("M7168_K2048_L4", 2, 152, 4),
+                                                 ("M7168_K16384_L1", 8, 152, 2),
+                                                 ("M4096_K7168_L8", 1, 512, 2)])
+def test_tensor_kernel_full_size(name, ks, ctas, stages):
     _, M, K, L = next(w for w in synthetic.WORKLOADS if w[0] == name)
     p = synthetic.make_problem(M, K, L, seed=0)
-    check(p, M, K, L, ks, ctas)
+    check(p, M, K, L, ks, ctas, stages)

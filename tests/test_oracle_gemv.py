@@ -295,3 +295,57 @@ def test_gemv_ex_brute_force_with_alpha_and_bias():
                               * _e2m1_fraction(bcode) * _e4m3_fraction(int(p["sfb"][l, k // 16])))
                 y = Fraction(float(alpha)) * total + Fraction(_half_value(int(bias[l, m])))
                 assert int(ce[l, m]) == fraction_to_fp16_bits(y), (case, l, m)
+
+
+def test_gemm_small_n_brute_force():
+    """Every (l, n, m) of the small-N GEMM against an exact Fraction sum over
+    b's row n, with an output scale and a bias."""
+    rng = np.random.default_rng(41)
+    for case in range(4):
+        M, N = int(rng.integers(1, 5)), int(rng.integers(2, 5))
+        K, L = 64 * int(rng.integers(1, 3)), int(rng.integers(1, 3))
+        a = rng.integers(0, 256, (L, M, K // 2), dtype=np.uint8)
+        b = rng.integers(0, 256, (L, N, K // 2), dtype=np.uint8)
+        sfa = (0x18 + rng.integers(0, 25, (L, M, K // 16))).astype(np.uint8)
+        sfb = (0x18 + rng.integers(0, 25, (L, N, K // 16))).astype(np.uint8)
+        alpha = [1.0, 0.75, -2.5, 0.1][case]
+        bias = None if case == 0 else (rng.standard_normal((L, N, M)) * 3).astype(
+            np.float16).view(np.uint16)
+        c, _, _ = oracle.gemm_small_n(a, b, sfa, sfb, M, N, K, L, alpha=alpha, bias=bias)
+        assert c.shape == (L, N, M)
+        for l in range(L):
+            for n in range(N):
+                for m in range(M):
+                    total = Fraction(0)
+                    for k in range(K):
+                        abyte, bbyte = int(a[l, m, k // 2]), int(b[l, n, k // 2])
+                        acode = (abyte >> 4) if k % 2 else (abyte & 15)
+                        bcode = (bbyte >> 4) if k % 2 else (bbyte & 15)
+                        total += (_e2m1_fraction(acode) * _e4m3_fraction(int(sfa[l, m, k // 16]))
+                                  * _e2m1_fraction(bcode) * _e4m3_fraction(int(sfb[l, n, k // 16])))
+                    y = Fraction(float(alpha)) * total
+                    if bias is not None:
+                        y += Fraction(_half_value(int(bias[l, n, m])))
+                    assert int(c[l, n, m]) == fraction_to_fp16_bits(y), (case, l, n, m)
+
+
+def test_gemm_small_n_with_one_vector_is_the_gemv():
+    M, K, L = 37, 320, 3
+    p = synthetic.make_problem(M, K, L, seed=8)
+    c, _, _ = oracle.gemm_small_n(p["a"], p["b"].reshape(L, 1, K // 2), p["sfa"],
+                                  p["sfb"].reshape(L, 1, K // 16), M, 1, K, L)
+    ref, _, _ = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
+    assert np.array_equal(c[:, 0, :], ref)
+
+
+def test_gemm_small_n_permuting_vectors_permutes_columns():
+    rng = np.random.default_rng(3)
+    M, N, K, L = 9, 5, 128, 2
+    a = rng.integers(0, 256, (L, M, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, (L, N, K // 2), dtype=np.uint8)
+    sfa = (0x18 + rng.integers(0, 25, (L, M, K // 16))).astype(np.uint8)
+    sfb = (0x18 + rng.integers(0, 25, (L, N, K // 16))).astype(np.uint8)
+    perm = rng.permutation(N)
+    c, _, _ = oracle.gemm_small_n(a, b, sfa, sfb, M, N, K, L)
+    cp, _, _ = oracle.gemm_small_n(a, b[:, perm], sfa, sfb[:, perm], M, N, K, L)
+    assert np.array_equal(cp, c[:, perm])
