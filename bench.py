@@ -527,6 +527,38 @@ def run_native(args):
                           "rotating_sets": ROTATE_SETS, "calls": wsteps}), flush=True)
         del wprob
         torch.cuda.empty_cache()
+        # the small-N GEMM (tensor-core kernel) on the decode-batch workloads;
+        # bytes = A + sfa + N x (b + sfb) read + N x c written
+        for gname, gM, gN, gK, gL in synthetic.GEMM_WORKLOADS:
+            gp = synthetic.make_gemm_problem(gM, gN, gK, gL, seed=0)
+            gbytes = synthetic.gemm_algorithmic_bytes(gM, gN, gK, gL)
+            gsets = max(2, min(ROTATE_SETS, -(-400 * 2 ** 20 // gbytes)))
+            a0 = torch.from_numpy(gp["a"]).to(dev)
+            b0 = torch.from_numpy(gp["b"]).to(dev)
+            sa0 = nv.repack_scales(torch.from_numpy(gp["sfa"]).to(dev))
+            sb0 = nv.repack_scales(torch.from_numpy(gp["sfb"]).to(dev))
+            gs = [(a0.clone(), b0.clone(), sa0.clone(), sb0.clone(),
+                   torch.empty(gL * gN * gM, dtype=torch.float16, device=dev)) for _ in range(gsets)]
+            del a0, b0, sa0, sb0
+
+            class _Gemm:
+                def call(self, nv_, i, h):
+                    x = gs[i % gsets]
+                    nv_.nvfp4_gemm_small_n(x[0].data_ptr(), x[1].data_ptr(), x[2].data_ptr(),
+                                           x[3].data_ptr(), x[4].data_ptr(), gM, gN, gK, gL,
+                                           stream=h)
+
+            gsteps = max(64, min(20000, int(2e9 / gbytes)) // 64 * 64)
+            gus, _, _ = time_graph(torch, nv, _Gemm(), gsteps, 64, stream)
+            gbs = gbytes / (gus * 1e-6) / 1e9
+            print(json.dumps({"workload": gname, "path": "nvfp4_gemm_small_n (tensor cores)",
+                              "N": gN, "us_per_call": round(gus, 3), "bytes_per_call": gbytes,
+                              "gb_per_s": round(gbs, 1),
+                              "pct_of_hbm_peak": round(100 * gbs / peaks["hbm_gbs"], 2),
+                              "rotating_sets": gsets, "calls": gsteps}), flush=True)
+            del gs
+            torch.cuda.empty_cache()
+        assert nv.nvfp4_tensor_wait_timeouts(reset=True) == 0, "a tensor-core pipeline wait ran out"
 
 
 def run_profile_case(args):

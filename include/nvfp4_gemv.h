@@ -207,6 +207,16 @@ nvfp4_status_t nvfp4_gemm_small_n_explicit(const void* a, const void* b, const v
                                            int64_t ctas, struct CUstream_st* stream);
 
 /*
+ * The tensor-core schedule nvfp4_gemm_small_n uses for N >= 2 (computed for
+ * any N in 1..16): stages per CTA, CTAs per cluster, grid size, and
+ * optionally (resident_ctas non-NULL) the CTAs of that kernel resident at once
+ * on the current device.  Queries the device (occupancy; cached per device).
+ */
+nvfp4_status_t nvfp4_gemm_small_n_plan(int64_t M, int64_t N, int64_t K, int64_t L,
+                                       int* stages, int* k_split, int64_t* ctas,
+                                       int* resident_ctas);
+
+/*
  * Scale repack: plain [L][rows][K/16] E4M3 -> the 128x4-atom pre-permuted
  * layout above (submission 69953, `to_blocked_batch`; submission 69575,
  * `blocked_transform_kernel`).  A byte permutation, bit-exact; padding rows

@@ -40,6 +40,7 @@ EXPORTS = (
     "nvfp4_tensor_wait_timeouts",
     "nvfp4_gemm_small_n",
     "nvfp4_gemm_small_n_explicit",
+    "nvfp4_gemm_small_n_plan",
 )
 
 
@@ -105,6 +106,10 @@ def library() -> ctypes.CDLL:
     lib.nvfp4_gemm_small_n.restype = I
     lib.nvfp4_gemm_small_n_explicit.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I, I, I64, P]
     lib.nvfp4_gemm_small_n_explicit.restype = I
+    lib.nvfp4_gemm_small_n_plan.argtypes = [I64, I64, I64, I64, ctypes.POINTER(I),
+                                            ctypes.POINTER(I), ctypes.POINTER(I64),
+                                            ctypes.POINTER(I)]
+    lib.nvfp4_gemm_small_n_plan.restype = I
     lib.nvfp4_tensor_wait_timeouts.argtypes = [I]
     lib.nvfp4_tensor_wait_timeouts.restype = I
     _lib = lib
@@ -162,6 +167,16 @@ def nvfp4_gemm_small_n_explicit(a: int, b: int, sfa: int, sfb: int, c: int, M: i
     _check(library().nvfp4_gemm_small_n_explicit(a, b, sfa, sfb, c, M, N, K, L, stages,
                                                  k_split, ctas, stream),
            "nvfp4_gemm_small_n_explicit")
+
+
+def nvfp4_gemm_small_n_plan(M: int, N: int, K: int, L: int) -> dict:
+    """The tensor-core schedule nvfp4_gemm_small_n uses (queries the device)."""
+    st, ks, ctas, res = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64(), ctypes.c_int()
+    _check(library().nvfp4_gemm_small_n_plan(M, N, K, L, ctypes.byref(st), ctypes.byref(ks),
+                                             ctypes.byref(ctas), ctypes.byref(res)),
+           "nvfp4_gemm_small_n_plan")
+    return {"stages": st.value, "k_split": ks.value, "ctas": ctas.value,
+            "resident_ctas": res.value}
 
 
 def nvfp4_repack_scales(src: int, dst: int, rows: int, K: int, L: int, stream: int = 0) -> None:

@@ -180,33 +180,31 @@ cudaError_t tc_resident_clusters(int stages, int64_t N, int ks, int* out) {
   return cudaSuccess;
 }
 
-// Tensor-core schedule: 2 stages per CTA (the most CTAs per SM, whose copy and
-// MMA chains overlap), and the cluster size that minimises the K stages of
-// the busiest CTA when the clusters that fit at once share the L*ceil(M/128)
-// tiles; ties go to the smaller cluster.
+// Tensor-core schedule (measured on GB300 over the decode-batch shapes): 2
+// stages per CTA, so the most CTAs share an SM and their copy+MMA chains
+// overlap; the smallest cluster size k_split whose L*ceil(M/128) tiles times
+// k_split fill at least 70% of the resident CTA slots, at least 2 once K has
+// 16 or more 256-element stages (shorter per-tile K ranges), at most 4 when
+// more than 8 columns are summed across the cluster, never more than the K
+// stages; and as many clusters as are resident at once (persistent), but no
+// more than the tiles.
 cudaError_t plan_tc(int64_t M, int64_t N, int64_t K, int64_t L, int* stages, int* k_split,
                     int64_t* ctas) {
   const int64_t tiles = L * ((M + 127) / 128);
   const int64_t kst = (K + 255) / 256;
   *stages = 2;
-  *k_split = 1;
-  *ctas = 1;
-  double best = -1.0;
-  for (int ks = 1; ks <= 8; ks *= 2) {
-    if (ks > 1 && ks > kst) break;
-    int resident = 0;
-    const cudaError_t err = tc_resident_clusters(2, N, ks, &resident);
-    if (err != cudaSuccess) return err;
-    const int64_t clusters = tiles < resident ? tiles : resident;
-    const int64_t per_cluster = (tiles + clusters - 1) / clusters;
-    const int64_t per_cta = (kst + ks - 1) / ks;
-    const double cost = (double)(per_cluster * (per_cta > 0 ? per_cta : 1));
-    if (best < 0.0 || cost < best - 1e-9) {
-      best = cost;
-      *k_split = ks;
-      *ctas = clusters * ks;
-    }
-  }
+  int slots = 0;
+  cudaError_t err = tc_resident_clusters(2, N, 1, &slots);
+  if (err != cudaSuccess) return err;
+  const int ks_max = N > 8 ? 4 : 8;
+  int ks = 1;
+  while (ks < ks_max && 2 * ks <= kst && tiles * ks * 10 < (int64_t)slots * 7) ks *= 2;
+  if (ks == 1 && kst >= 16) ks = 2;
+  int resident = 0;
+  err = tc_resident_clusters(2, N, ks, &resident);
+  if (err != cudaSuccess) return err;
+  *k_split = ks;
+  *ctas = (tiles < resident ? tiles : resident) * ks;
   return cudaSuccess;
 }
 
@@ -528,6 +526,21 @@ nvfp4_status_t nvfp4_gemm_small_n_explicit(const void* a, const void* b, const v
   if (M == 0 || N == 0 || L == 0) return NVFP4_OK;
   return run_gemm_tc(a, b, sfa, sfb, c, M, N, K, L, stages, k_split, ctas, kDefaultOptions,
                      (cudaStream_t)stream);
+}
+
+nvfp4_status_t nvfp4_gemm_small_n_plan(int64_t M, int64_t N, int64_t K, int64_t L,
+                                       int* stages, int* k_split, int64_t* ctas,
+                                       int* resident_ctas) {
+  if (stages == nullptr || k_split == nullptr || ctas == nullptr) return NVFP4_ERR_INVALID_VALUE;
+  nvfp4_status_t st = validate_gemm(nullptr, nullptr, nullptr, nullptr, nullptr, 0, N, K, L,
+                                    kDefaultOptions);
+  if (st != NVFP4_OK) return st;
+  if (M < 0 || M > kMaxM || (M != 0 && L > kMaxRows / M)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  cudaError_t err = plan_tc(M, N < 1 ? 1 : N, K, L, stages, k_split, ctas);
+  if (err == cudaSuccess && resident_ctas != nullptr)
+    err = tc_resident_clusters(2, N < 1 ? 1 : N, 1, resident_ctas);
+  if (err != cudaSuccess) return cuda_failure(err);
+  return NVFP4_OK;
 }
 
 int nvfp4_last_cuda_error(void) { return g_last_cuda_error; }

@@ -559,6 +559,11 @@ cudaError_t tc_launch_config(TcKernel kern, int stages, int nc, cudaLaunchConfig
   const uint32_t smem = tc_smem_bytes(stages, nc);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
+  // all of the unified L1/shared storage as shared memory: the kernel reads
+  // nothing through L1, and more CTAs per SM overlap their copy+MMA chains
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  if (err != cudaSuccess) return err;
   cfg = {};
   cfg.gridDim = dim3((unsigned)ctas, 1, 1);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
@@ -634,8 +639,33 @@ cudaError_t tc_max_active_clusters(int stages, int64_t N, int ks, int* out) {
   cudaLaunchAttribute attr[2];
   cudaError_t err = tc_launch_config(kern, stages, nc, cfg, attr, ks, ks, nullptr);
   if (err != cudaSuccess) return err;
-  cfg.numAttrs = 1;  // the cluster shape alone
-  return cudaOccupancyMaxActiveClusters(out, kern, &cfg);
+  // CTAs per SM from the per-CTA limits: shared memory (with the per-CTA
+  // reservation), registers, threads, and TMEM (512 columns per SM).  The
+  // occupancy queries answer one CTA per SM for this kernel, while measured
+  // runs place several per SM (twice the throughput with two).
+  cudaFuncAttributes fa;
+  err = cudaFuncGetAttributes(&fa, kern);
+  if (err != cudaSuccess) return err;
+  int dev = 0, sms = 0, smem_sm = 0, reserved = 0, regs_sm = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess ||
+      (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+      (err = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+          cudaSuccess ||
+      (err = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+          cudaSuccess ||
+      (err = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) !=
+          cudaSuccess)
+    return err;
+  const int smem_cta = (int)tc_smem_bytes(stages, nc) + (int)fa.sharedSizeBytes + reserved;
+  const int regs_cta = ((fa.numRegs * 32 + 255) / 256 * 256) * (kTcThreads / 32);
+  int per_sm = smem_sm / smem_cta;
+  if (regs_cta > 0 && regs_sm / regs_cta < per_sm) per_sm = regs_sm / regs_cta;
+  if (2048 / kTcThreads < per_sm) per_sm = 2048 / kTcThreads;
+  const int by_tmem = 512 / (int)tc_tmem_cols(stages);
+  if (by_tmem < per_sm) per_sm = by_tmem;
+  if (per_sm < 1) per_sm = 1;
+  *out = sms * per_sm / ks > 0 ? sms * per_sm / ks : 1;
+  return cudaSuccess;
 }
 
 cudaError_t tc_wait_timeouts(int reset, int* out) {

@@ -413,3 +413,13 @@ def test_gemm_small_n_validation(lib):
     assert E(*args, 2, 1, 0, None) == nv.ERR_INVALID_VALUE
     assert E(*(ptrs + (300, 4, 0, 2)), 2, 2, 2, None) == nv.ERR_INVALID_VALUE  # K = 0: no split
     assert E(*(ptrs + (0, 4, 1024, 2)), 2, 1, 1, None) == nv.OK
+
+
+def test_gemm_small_n_plan_validation(lib):
+    st, ks, ctas, res = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64(), ctypes.c_int()
+    args = (ctypes.byref(st), ctypes.byref(ks), ctypes.byref(ctas), ctypes.byref(res))
+    assert lib.nvfp4_gemm_small_n_plan(300, 17, 1024, 2, *args) == nv.ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_gemm_small_n_plan(300, 4, 1000, 2, *args) == nv.ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_gemm_small_n_plan(-1, 4, 1024, 2, *args) == nv.ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_gemm_small_n_plan(300, 4, 1024, 2, None, None, None, None) == \
+        nv.ERR_INVALID_VALUE
