@@ -64,6 +64,9 @@ def parse_args():
     ap.add_argument("--schedule", default=None,
                     help="with --ncu: KERNEL,LANES_PER_ROW,K_SPLIT,CTAS for nvfp4_gemv_explicit "
                          "instead of the chosen schedule")
+    ap.add_argument("--gemm-workload", default=None,
+                    help="with --ncu: run nvfp4_gemm_small_n on this decode-batch workload "
+                         "(e.g. M7168_N8_K2048_L4) instead of the GEMV")
     ap.add_argument("--repack", action="store_true",
                     help="with --ncu: run the scale repack of --workload's sfa instead of the GEMV")
     return ap.parse_args()
@@ -570,6 +573,24 @@ def run_profile_case(args):
 
     libbuild.build()
     dev = torch.device("cuda", 0)
+    if args.gemm_workload:
+        gname, gM, gN, gK, gL = next(w for w in synthetic.GEMM_WORKLOADS
+                                     if w[0] == args.gemm_workload)
+        gp = synthetic.make_gemm_problem(gM, gN, gK, gL, seed=0)
+        a = torch.from_numpy(gp["a"]).to(dev)
+        b = torch.from_numpy(gp["b"]).to(dev)
+        sfa = nv.repack_scales(torch.from_numpy(gp["sfa"]).to(dev))
+        sfb = nv.repack_scales(torch.from_numpy(gp["sfb"]).to(dev))
+        c = torch.empty(gL * gN * gM, dtype=torch.float16, device=dev)
+        gstream = torch.cuda.Stream(device=dev)
+        torch.cuda.synchronize()
+        for _ in range(args.warmup + args.steps):
+            nv.nvfp4_gemm_small_n(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(),
+                                  c.data_ptr(), gM, gN, gK, gL, stream=gstream.cuda_stream)
+        gstream.synchronize()
+        assert nv.nvfp4_tensor_wait_timeouts(reset=True) == 0
+        print(f"profile case done: {gname} small-N GEMM {args.warmup}+{args.steps} calls")
+        return
     name, M, K, L = next(w for w in synthetic.WORKLOADS if w[0] == args.workload)
     layout = nv.SF_PLAIN if args.layout == "plain" else nv.SF_PERMUTED_128x4
     p = synthetic.make_problem(M, K, L, seed=0)
