@@ -12,19 +12,24 @@
 // one sfa atom and one sfb atom (512 B each) feed one MMA.  (An MMA's scale
 // address in TMEM is a 4-column-aligned copy destination.)
 //
-// One CTA (192 threads):
+// One CTA (224 threads):
 //   warp 0      one lane issues the copies of each 256-element K stage: A as
 //               a 128-row x 128-byte TMA tile (128-byte swizzle), b as an
 //               N-row TMA tile, and the stage's 4 sfa atoms and 4 sfb atoms as
 //               two 2 KB bulk copies (consecutive atoms are adjacent);
-//   warp 1      allocates TMEM; one lane copies the stage's 8 atoms into TMEM
-//               (tcgen05.cp) and issues its MMAs, then
-//               commits the stage back to the producer and, at the end of a
-//               tile, the (double-buffered) accumulator to the epilogue;
-//   warps 2..5  read the accumulator (one TMEM lane quarter each), and either
-//               store c or hand their partial sums to the cluster's rank 0.
-// The copies and MMAs of one stage complete one after another; a CTA has 2 or
-// 4 stages and several CTAs share an SM, whose independent chains overlap.
+//   warps 1, 6  two independent MMA chains (warp 1 also allocates TMEM):
+//               chain c takes the stages i with i % 2 == c of every tile,
+//               through a ring of its own, into its own (double-buffered)
+//               accumulator; one lane copies the stage's 8 atoms into TMEM
+//               (tcgen05.cp) and issues its MMAs, then commits the stage back
+//               to the producer and, at the end of a tile, the accumulator to
+//               the epilogue;
+//   warps 2..5  read and add the two accumulators (one TMEM lane quarter each),
+//               and either store c or hand their partial sums to the cluster's
+//               rank 0.
+// The copies and MMAs of one chain complete one after another; a CTA has two
+// chains of 1 or 2 stages each, and several CTAs share an SM, so independent
+// chains overlap.
 // Split K: the KS CTAs of a cluster share every tile, each taking a
 // contiguous range of 256-element K stages (the rank that takes an extra
 // stage rotates from tile to tile); ranks 1..KS-1 leave their partial sums
@@ -54,20 +59,20 @@ __device__ int g_tc_timeouts;
 
 namespace {
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 224;  // 7 warps
 constexpr uint32_t kTcABytes = 128 * 128;   // 128 rows x 256 elements
 constexpr uint32_t kTcBBytes = 16 * 128;    // 16 rows x 256 elements (rows 0..N-1 = b)
 constexpr uint32_t kTcSfBytes = 4 * 512;    // 4 scale atoms (K = 256)
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s
 
-// TMEM columns a CTA allocates: accumulators [2][16], then sfa and sfb
-// [stage][4 atoms][4 columns] each (a power of two, at least 32).
+// TMEM columns a CTA allocates: accumulators [2 chains][2][16], then sfa and
+// sfb [stage][4 atoms][4 columns] each (a power of two, at least 32).
 __host__ __device__ constexpr uint32_t tc_tmem_cols(int stages) { return stages <= 2 ? 128u : 256u; }
 constexpr uint32_t tc_smem_bytes(int stages, int nc) {
   return (uint32_t)stages * (kTcABytes + kTcBBytes + 2 * kTcSfBytes) +
          2u * (uint32_t)nc * 128u * 4u + 1024u;
 }
-static_assert(32 + 32 * 2 <= tc_tmem_cols(2) && 32 + 32 * 4 <= tc_tmem_cols(4), "TMEM columns");
+static_assert(64 + 32 * 2 <= tc_tmem_cols(2) && 64 + 32 * 4 <= tc_tmem_cols(4), "TMEM columns");
 // The SM's 512 TMEM columns are never oversubscribed, so an allocation never
 // waits for another CTA: shared memory (228 KB per SM, 1 KB of it reserved
 // per CTA) admits at most 4 CTAs of 2 stages (128 columns), at most 2 of 4
@@ -317,8 +322,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t rfull_bar = bar0 + 8u * (2 * S + 4);   // [2] (rank 0)
   const uint32_t rfree_bar = bar0 + 8u * (2 * S + 6);   // [2] (ranks > 0)
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 8);
-  // TMEM columns: accumulators [2][16], sfa and sfb [stage][4 atoms][4]
-  constexpr uint32_t kSfaCol = 32, kSfbCol = 32 + 16 * S, kTmemCols = tc_tmem_cols(S);
+  // TMEM columns: accumulators [2 chains][2][16], sfa and sfb [stage][4 atoms][4]
+  constexpr uint32_t kSfaCol = 64, kSfbCol = 64 + 16 * S, kTmemCols = tc_tmem_cols(S);
+  // stage slots per MMA chain: chain c owns slots c*SC .. c*SC + SC - 1
+  constexpr int SC = S / 2;
+  static_assert(S % 2 == 0, "two chains of equal rings");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ks = cluster_size(), rank = cluster_rank();
@@ -332,12 +340,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(empty_bar(st), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(dfull_bar + 8u * i, 1);
+      mbar_init(dfull_bar + 8u * i, 2);  // one commit per MMA chain
       mbar_init(dempty_bar + 8u * i, 128);
       mbar_init(rfull_bar + 8u * i, ks > 1 ? (ks - 1) * 128 : 1);
       mbar_init(rfree_bar + 8u * i, 128);
     }
-    mbar_init(drain_bar, 1);
+    mbar_init(drain_bar, 2);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   // rows N..15 of every B stage start as zeros and are never written again
@@ -371,7 +379,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   };
 
   if (warp == 0) {
-    int issued = 0;
     if (lane == 0) {
       if (ntiles > 0) {  // the first stages' A lines, ahead of the dependency wait
         int s0, cnt;
@@ -381,8 +388,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tma_prefetch_3d(&p.tmap_a, (s0 + i) * 128, mt * 128, l);
       }
       pdl_wait();
-      int st = 0;
-      uint32_t ph = 0;
+      // stage i of a tile goes to MMA chain i % 2, through that chain's ring
+      int pos[2] = {0, 0}, issued[2] = {0, 0};
+      uint32_t ph[2] = {0u, 0u};
       for (int j = 0; j < ntiles; ++j) {
         const int t = cid + j * nclusters;
         const int l = t / p.rest_m, mt = t % p.rest_m;
@@ -391,7 +399,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int i = 0; i < cnt; ++i) {
           const int s = s0 + i;
           const int nk = min(4, p.rest_k - 4 * s);
-          if (mbar_wait<false>(empty_bar(st), ph ^ 1u, ok)) {
+          const int c = i & 1, st = c * SC + pos[c];
+          if (mbar_wait<false>(empty_bar(st), ph[c] ^ 1u, ok)) {
             const uint32_t fb = full_bar(st);
             mbar_expect_tx(fb, kTcABytes + 128u * (uint32_t)p.N + 2u * (uint32_t)nk * 512u);
             tma_load_3d(a_s + st * kTcABytes, &p.tmap_a, s * 128, mt * 128, l, fb);
@@ -401,37 +410,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       (uint32_t)nk * 512u, fb);
             bulk_load(sfb_s + st * kTcSfBytes, p.sfb + (int64_t)l * p.sfb_stride + (int64_t)s * 2048,
                       (uint32_t)nk * 512u, fb);
-            ++issued;
+            ++issued[c];
           }
-          if (++st == S) {
-            st = 0;
-            ph ^= 1u;
+          if (++pos[c] == SC) {
+            pos[c] = 0;
+            ph[c] ^= 1u;
           }
         }
       }
       // copies still in flight land before the CTA can exit: the last phase
-      // issued on each stage (a phase already consumed passes at once)
+      // issued on each slot (a phase already consumed passes at once)
       bool drain_ok = true;
-      for (int k = 0; k < S && k < issued; ++k) {
-        const int i_last = issued - 1 - k;
-        mbar_wait<false>(full_bar(i_last % S), (uint32_t)((i_last / S) & 1), drain_ok);
-      }
+      for (int c = 0; c < 2; ++c)
+        for (int k = 0; k < SC && k < issued[c]; ++k) {
+          const int i_last = issued[c] - 1 - k;
+          mbar_wait<false>(full_bar(c * SC + i_last % SC), (uint32_t)((i_last / SC) & 1), drain_ok);
+        }
     } else {
       pdl_wait();
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 6) {
+    // MMA chain c takes the stages i with i % 2 == c of every tile into its own
+    // accumulator; the two chains' copies and MMAs run independently
     pdl_wait();
-    int st = 0;
+    const int c = warp == 1 ? 0 : 1;
+    int pos = 0;
     uint32_t ph = 0;
     for (int j = 0; j < ntiles; ++j) {
       const int acc = j & 1;
-      const uint32_t d = tmem + (uint32_t)(16 * acc);
+      const uint32_t d = tmem + (uint32_t)(16 * (2 * c + acc));
       if (lane == 0) mbar_wait<false>(dempty_bar + 8u * acc, ((uint32_t)(j >> 1) & 1u) ^ 1u, ok);
       int s0, cnt;
       stage_range(cid + j * nclusters, s0, cnt);
-      for (int i = 0; i < cnt; ++i) {
+      bool first = true;
+      for (int i = c; i < cnt; i += 2) {
         const int s = s0 + i;
         const int nk = min(4, p.rest_k - 4 * s);
+        const int st = c * SC + pos;
         if (lane == 0 && mbar_wait<false>(full_bar(st), ph, ok)) {
           tc_fence_after();
           for (int kk = 0; kk < nk; ++kk) {
@@ -444,18 +459,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_mma(d, desc_sw128(a_s + st * kTcABytes + 32u * kk),
                    desc_sw128(b_s + st * kTcBBytes + 32u * kk),
                    tmem + kSfaCol + (uint32_t)(16 * st + 4 * kk),
-                   tmem + kSfbCol + (uint32_t)(16 * st + 4 * kk), i > 0 || kk > 0);
+                   tmem + kSfbCol + (uint32_t)(16 * st + 4 * kk), !first || kk > 0);
           tc_commit(empty_bar(st));
         }
-        if (++st == S) {
-          st = 0;
+        first = false;
+        if (++pos == SC) {
+          pos = 0;
           ph ^= 1u;
         }
       }
+      // a chain with no stage in this tile commits at once (its accumulator is
+      // not read)
       if (lane == 0 && ok) tc_commit(dfull_bar + 8u * acc);
     }
     if (lane == 0) {
-      // every MMA and TMEM copy has finished before TMEM is released
+      // every MMA and TMEM copy of this chain has finished before TMEM is released
       tc_commit(drain_bar);
       bool drain_ok = true;
       mbar_wait<false>(drain_bar, 0, drain_ok);
@@ -475,9 +493,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float part[NC];
 #pragma unroll
       for (int n = 0; n < NC; ++n) part[n] = 0.f;
-      if (ok && p.kstages > 0) {  // K = 0: the sums are zero and no MMA ran
+      int s0, cnt;
+      stage_range(t, s0, cnt);
+      if (ok && cnt > 0) {  // K = 0: the sums are zero and no MMA ran
         tc_fence_after();
         tmem_load_cols<NC>(tmem + (uint32_t)(16 * acc) + ((32u * q) << 16), part);
+        if (cnt > 1) {  // chain 1 took the odd stages
+          float odd[NC];
+          tmem_load_cols<NC>(tmem + (uint32_t)(16 * (2 + acc)) + ((32u * q) << 16), odd);
+#pragma unroll
+          for (int n = 0; n < NC; ++n) part[n] += odd[n];
+        }
       }
       tc_fence_before();
       mbar_arrive(dempty_bar + 8u * acc);
