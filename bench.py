@@ -481,7 +481,10 @@ def run_native(args):
                 wus, _, _ = time_graph(torch, nv, wprob, wsteps, 64, stream)
                 smed, smin = time_single_flushed(torch, nv, wprob, 20, stream)
                 gbs = wbytes / (wus * 1e-6) / 1e9
-                print(json.dumps({"workload": wname, "scale_layout": lay_name,
+                kname = ["direct", "pipelined", "tensor"][
+                    nv.nvfp4_gemv_plan(wM, wK, wL, lay, num_sms=torch.cuda.get_device_properties(
+                        dev).multi_processor_count)["kernel"]]
+                print(json.dumps({"workload": wname, "scale_layout": lay_name, "kernel": kname,
                                   "us_per_call": round(wus, 3), "gb_per_s": round(gbs, 1),
                                   "pct_of_hbm_peak": round(100 * gbs / peaks["hbm_gbs"], 2),
                                   "rotating_sets": sets, "calls": wsteps,

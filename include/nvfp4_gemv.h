@@ -151,7 +151,9 @@ typedef enum {
    * persistent over the L*ceil(M/128) tiles); lanes_per_row = pipeline
    * stages per CTA (2 or 4: 4, 3 or 2 CTAs of 2 stages share an SM, 2 of 4).
    * The MMA sums in fp32 in an order of its own: c meets the same accuracy
-   * contract, not the CUDA-core kernels' bits. */
+   * contract, not the CUDA-core kernels' bits.  nvfp4_gemv picks it for
+   * pre-permuted scales with at least 512 MB of A (where it streams faster);
+   * the pipelined kernel otherwise. */
   NVFP4_KERNEL_TENSOR = 2
 } nvfp4_kernel_t;
 

@@ -187,24 +187,36 @@ cudaError_t tc_resident_clusters(int stages, int64_t N, int ks, int* out) {
 // 16 or more 256-element stages (shorter per-tile K ranges), at most 4 when
 // more than 8 columns are summed across the cluster, never more than the K
 // stages; and as many clusters as are resident at once (persistent), but no
-// more than the tiles.
-cudaError_t plan_tc(int64_t M, int64_t N, int64_t K, int64_t L, int* stages, int* k_split,
-                    int64_t* ctas) {
+// more than the tiles.  slots = CTAs resident at once.
+void tc_rule(int64_t M, int64_t N, int64_t K, int64_t L, int64_t slots, int* stages,
+             int* k_split, int64_t* ctas) {
   const int64_t tiles = L * ((M + 127) / 128);
   const int64_t kst = (K + 255) / 256;
-  *stages = 2;
-  int slots = 0;
-  cudaError_t err = tc_resident_clusters(2, N, 1, &slots);
-  if (err != cudaSuccess) return err;
   const int ks_max = N > 8 ? 4 : 8;
   int ks = 1;
-  while (ks < ks_max && 2 * ks <= kst && tiles * ks * 10 < (int64_t)slots * 7) ks *= 2;
+  while (ks < ks_max && 2 * ks <= kst && tiles * ks * 10 < slots * 7) ks *= 2;
   if (ks == 1 && kst >= 16) ks = 2;
-  int resident = 0;
-  err = tc_resident_clusters(2, N, ks, &resident);
-  if (err != cudaSuccess) return err;
+  const int64_t resident = slots / ks > 0 ? slots / ks : 1;
+  *stages = 2;
   *k_split = ks;
   *ctas = (tiles < resident ? tiles : resident) * ks;
+}
+
+// The GEMV (N = 1) on the tensor-core kernel instead of the pipelined
+// CUDA-core kernel: pre-permuted scales and at least 512 MB of A.  Measured on
+// GB300: 177 us against 182-190 us on M16384_K8192_L16 (1.07 GB of A), level
+// on M4096_K7168_L8 (117 MB), slower below.
+bool tensor_gemv_pays(int64_t M, int64_t K, int64_t L, bool permuted) {
+  return permuted && K > 0 && M * L * (K / 2) >= (int64_t(1) << 29);
+}
+
+// The rule above with the CTAs of the 2-stage kernel resident on this device.
+cudaError_t plan_tc(int64_t M, int64_t N, int64_t K, int64_t L, int* stages, int* k_split,
+                    int64_t* ctas) {
+  int slots = 0;
+  const cudaError_t err = tc_resident_clusters(2, N, 1, &slots);
+  if (err != cudaSuccess) return err;
+  tc_rule(M, N, K, L, slots, stages, k_split, ctas);
   return cudaSuccess;
 }
 
@@ -252,6 +264,7 @@ nvfp4_status_t run_gemm_tc(const void* a, const void* b, const void* sfa, const 
 }  // namespace
 
 int rows_per_pass(const GemvPlan& plan) {
+  if (plan.kernel == kKernelTensor) return 128;  // one tile of A rows
   return plan.kernel == kKernelAsync ? kAsyncItems * (32 / plan.lanes_per_row) * plan.groups
                                      : kRowsPerPass;
 }
@@ -329,9 +342,27 @@ int async_groups(int64_t M, int64_t L, bool permuted, int lanes_per_row, int k_s
 bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int num_sms,
                int ctas_per_sm, GemvPlan* out) {
   if (M < 0 || K < 0 || L < 0 || num_sms < 1 || ctas_per_sm < 1 || out == nullptr) return false;
-  if (kernel < -1 || kernel > kKernelAsync) return false;
+  if (kernel < -1 || kernel > kKernelTensor) return false;
   const int64_t kchunks = K / 64;
-  if (kernel == -1) kernel = kchunks > 0 ? kKernelAsync : kKernelDirect;
+  if (kernel == -1)
+    kernel = tensor_gemv_pays(M, K, L, permuted) ? kKernelTensor
+             : kchunks > 0                       ? kKernelAsync
+                                                 : kKernelDirect;
+  if (kernel == kKernelTensor) {
+    if (!permuted || kchunks == 0) return false;
+    // host-only estimate: 4 CTAs of the 2-stage kernel resident per SM
+    // (the launch recomputes the schedule from this device's limits)
+    int stages = 2, ks = 1;
+    int64_t ctas = 1;
+    tc_rule(M, 1, K, L, (int64_t)num_sms * 4, &stages, &ks, &ctas);
+    out->kernel = kKernelTensor;
+    out->lanes_per_row = stages;
+    out->k_split = ks;
+    out->groups = 1;
+    out->ctas = ctas;
+    out->steps = (K + 255) / 256;
+    return true;
+  }
   if (kernel == kKernelAsync && kchunks == 0) return false;
   const int64_t rows = M * L;
   int64_t ctas = (int64_t)num_sms * ctas_per_sm;
@@ -419,6 +450,15 @@ nvfp4_status_t nvfp4_gemv_ex(const void* a, const void* b, const void* sfa, cons
   GemvPlan plan;
   if (!plan_gemv(M, K, L, sf_layout == NVFP4_SF_PERMUTED_128x4, -1, sms, occ, &plan))
     return NVFP4_ERR_INVALID_VALUE;
+  if (plan.kernel == kKernelTensor) {
+    int stages = 2, ks = 1;
+    int64_t ctas = 1;
+    err = plan_tc(M, 1, K, L, &stages, &ks, &ctas);
+    if (err != cudaSuccess) return cuda_failure(err);
+    plan.lanes_per_row = stages;
+    plan.k_split = ks;
+    plan.ctas = ctas;
+  }
   return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, opt, (cudaStream_t)stream);
 }
 
@@ -562,7 +602,7 @@ nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, i
   nvfp4_status_t st = validate_gemv_shape(M, K, L, sf_layout);
   if (st != NVFP4_OK) return st;
   GemvPlan plan;
-  if (kernel < -1 || kernel > kKernelAsync) return NVFP4_ERR_INVALID_VALUE;
+  if (kernel < -1 || kernel > kKernelTensor) return NVFP4_ERR_INVALID_VALUE;
   if (!plan_gemv(M, K, L, sf_layout == NVFP4_SF_PERMUTED_128x4, kernel, num_sms,
                  ctas_per_sm > 0 ? ctas_per_sm : kGemvMinCtasPerSm, &plan))
     return NVFP4_ERR_UNSUPPORTED_SHAPE;
@@ -570,7 +610,7 @@ nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, i
   out->lanes_per_row = plan.lanes_per_row;
   out->k_split = plan.k_split;
   out->rows_per_pass = rows_per_pass(plan);
-  out->threads_per_cta = kGemvThreads;
+  out->threads_per_cta = plan.kernel == kKernelTensor ? kTcThreadsPerCta : kGemvThreads;
   out->ctas = plan.ctas;
   out->steps = plan.steps;
   return NVFP4_OK;

@@ -59,7 +59,7 @@ __device__ int g_tc_timeouts;
 
 namespace {
 
-constexpr int kTcThreads = 224;  // 7 warps
+constexpr int kTcThreads = kTcThreadsPerCta;  // 7 warps
 constexpr uint32_t kTcABytes = 128 * 128;   // 128 rows x 256 elements
 constexpr uint32_t kTcBBytes = 16 * 128;    // 16 rows x 256 elements (rows 0..N-1 = b)
 constexpr uint32_t kTcSfBytes = 4 * 512;    // 4 scale atoms (K = 256)

@@ -76,6 +76,8 @@ cudaError_t repack_ctas_per_sm(int* out);
 cudaError_t launch_repack(const uint8_t* src, uint8_t* dst, int64_t rows, int64_t K, int64_t L,
                           int64_t max_ctas, cudaStream_t stream);
 
+constexpr int kTcThreadsPerCta = 224;  // tensor-core kernel: 7 warps
+
 // Tensor-core kernel (gemv_tc.cu, pre-permuted scales): N (1..16) rows of b
 // (row n at b + l*p.b_stride + n*b_row_stride), c [L][N][M]; stages (2 or 4)
 // per CTA; ctas CTAs in clusters of ks, each cluster splitting a 128-row

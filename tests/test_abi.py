@@ -145,7 +145,8 @@ BENCH_SHAPES = [(128, 256, 1), (7168, 2048, 4), (4096, 7168, 8), (7168, 16384, 1
     (BENCH_SHAPES[1], 1, -1, (1, 4, 4, 304, 64)),
     (BENCH_SHAPES[2], 1, -1, (1, 16, 1, 304, 16)),
     (BENCH_SHAPES[3], 1, -1, (1, 16, 8, 304, 32)),
-    (BENCH_SHAPES[4], 1, -1, (1, 4, 8, 304, 64)),
+    (BENCH_SHAPES[4], 1, -1, (2, 2, 2, 608, 128)),  # >= 512 MB of A: tensor cores
+    (BENCH_SHAPES[4], 1, 1, (1, 4, 8, 304, 64)),
     (BENCH_SHAPES[0], 0, 0, (0, 4, 1, 64, 8)),
     (BENCH_SHAPES[1], 0, 0, (0, 32, 1, 304, 8)),
     (BENCH_SHAPES[2], 0, 0, (0, 16, 1, 304, 8)),
@@ -157,7 +158,32 @@ def test_plan_for_the_benchmark_shapes(lib, shape, layout, kernel, want):
     plan = nv.nvfp4_gemv_plan(M, K, L, layout, num_sms=152, ctas_per_sm=2, kernel=kernel)
     got = tuple(plan[k] for k in ("kernel", "lanes_per_row", "k_split", "ctas", "rows_per_pass"))
     assert got == want
-    assert plan["steps"] == -(-(K // 64) // plan["lanes_per_row"])
+    if plan["kernel"] == nv.KERNEL_TENSOR:  # lanes_per_row = stages; steps = 256-element K stages
+        assert plan["steps"] == -(-K // 256) and plan["threads_per_cta"] == 224
+    else:
+        assert plan["steps"] == -(-(K // 64) // plan["lanes_per_row"])
+
+
+def test_tensor_kernel_plans(lib):
+    """The tensor-core kernel: pre-permuted scales only; chosen by default for
+    GEMVs with at least 512 MB of A; its schedule follows the measured rule
+    (2 stages, the smallest cluster filling 70% of 4 resident CTAs per SM, at
+    least 2 for 16+ K stages, persistent clusters no more than the tiles)."""
+    with pytest.raises(nv.Nvfp4Error):
+        nv.nvfp4_gemv_plan(4096, 7168, 8, 0, 152, 2, kernel=nv.KERNEL_TENSOR)
+    assert nv.nvfp4_gemv_plan(16384, 8192, 16, 0, 152, 2)["kernel"] == nv.KERNEL_PIPELINED
+    assert nv.nvfp4_gemv_plan(16384, 8192, 2, 1, 152, 2)["kernel"] == nv.KERNEL_PIPELINED
+    assert nv.nvfp4_gemv_plan(16384, 8192, 8, 1, 152, 2)["kernel"] == nv.KERNEL_TENSOR
+    rng = np.random.default_rng(1)
+    for _ in range(200):
+        M, K, L = int(rng.integers(1, 30000)), 64 * int(rng.integers(1, 400)), int(rng.integers(1, 9))
+        sms = int(rng.integers(1, 200))
+        plan = nv.nvfp4_gemv_plan(M, K, L, 1, sms, 2, kernel=nv.KERNEL_TENSOR)
+        tiles, kst = L * -(-M // 128), -(-K // 256)
+        ks = plan["k_split"]
+        assert plan["lanes_per_row"] == 2 and ks in (1, 2, 4, 8) and (ks == 1 or ks <= kst)
+        assert plan["ctas"] % ks == 0 and plan["ctas"] // ks <= tiles
+        assert plan["ctas"] <= max(ks, 4 * sms)
 
 
 def max_rows_per_row_lane(M, L, perm, lpr, ks, ctas):
@@ -179,7 +205,7 @@ def test_pipelined_rows_per_pass_cover_the_longest_range(lib):
         M, L = int(rng.integers(1, 30000)), int(rng.integers(1, 17))
         K = 64 * int(rng.integers(1, 300))
         layout = int(rng.integers(0, 2))
-        plan = nv.nvfp4_gemv_plan(M, K, L, layout, 152, 2)
+        plan = nv.nvfp4_gemv_plan(M, K, L, layout, 152, 2, kernel=nv.KERNEL_PIPELINED)
         nr = 4 * (32 // plan["lanes_per_row"])
         rows = max_rows_per_row_lane(M, L, layout == 1, plan["lanes_per_row"], plan["k_split"],
                                      plan["ctas"])
@@ -193,7 +219,8 @@ def test_permuted_plans_avoid_half_sector_scale_reads(lib):
     for _ in range(200):
         M, L = int(rng.integers(1, 30000)), int(rng.integers(1, 17))
         K = 64 * int(rng.integers(1, 300))
-        assert nv.nvfp4_gemv_plan(M, K, L, nv.SF_PERMUTED_128x4, 152, 2)["lanes_per_row"] != 32
+        assert nv.nvfp4_gemv_plan(M, K, L, nv.SF_PERMUTED_128x4, 152, 2,
+                                  kernel=nv.KERNEL_PIPELINED)["lanes_per_row"] != 32
 
 
 def test_permuted_plans_with_plenty_of_rows_use_narrow_rows(lib):
