@@ -327,9 +327,13 @@ int async_groups(int64_t M, int64_t L, bool permuted, int lanes_per_row, int k_s
 // means):
 //  * kernel: the pipelined (cp.async) kernel for every K > 0; the direct
 //    kernel writes the zeros of K == 0;
+//  * tiny problems with plain scales (up to 512 KB of A): the direct kernel,
+//    rows narrow enough for at most 4 K steps, those steps split over warps,
+//    one CTA per 8 KB of A (measured, see above);
 //  * ctas: one wave of resident CTAs (SMs x occupancy), fewer for tiny
 //    problems (at least 2 rows per CTA: short, long-K problems still spread
-//    their K splits over many SMs);
+//    their K splits over many SMs), and at most 64 for the pipelined kernel
+//    on plain scales up to 2 MB of A;
 //  * pipelined kernel: (lanes_per_row, k_split) minimising the cost model
 //    above over 32/16/8/4 lanes (16/8/4 for permuted scales) and splits
 //    1..8 no larger than the chunk steps (ties go to the wider row, then the
@@ -344,10 +348,20 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
   if (M < 0 || K < 0 || L < 0 || num_sms < 1 || ctas_per_sm < 1 || out == nullptr) return false;
   if (kernel < -1 || kernel > kKernelTensor) return false;
   const int64_t kchunks = K / 64;
+  const int64_t a_bytes = M * L * (K / 2);
+  // Tiny problems with plain scales (measured on GB300 over 16 KB .. 2 MB of
+  // A): the launch and the first DRAM access dominate, and fewer, fuller CTAs
+  // finish first.  Up to 512 KB the direct kernel does best with rows narrow
+  // enough for at most 4 K steps, those steps split over warps and one CTA
+  // per 8 KB of A (e.g. M128_K256_L1: 1.50 against 1.73 us); up to 2 MB the
+  // pipelined kernel does best on at most 64 CTAs.  (Pre-permuted scales keep
+  // the general schedule: the same rule was slower for some of them.)
+  const bool small_plain = !permuted && kchunks > 0 && a_bytes <= (int64_t(2) << 20);
+  const bool tiny = kernel == -1 && small_plain && a_bytes <= (int64_t(512) << 10);
   if (kernel == -1)
     kernel = tensor_gemv_pays(M, K, L, permuted) ? kKernelTensor
-             : kchunks > 0                       ? kKernelAsync
-                                                 : kKernelDirect;
+             : tiny || kchunks == 0              ? kKernelDirect
+                                                 : kKernelAsync;
   if (kernel == kKernelTensor) {
     if (!permuted || kchunks == 0) return false;
     // host-only estimate: 4 CTAs of the 2-stage kernel resident per SM
@@ -368,8 +382,28 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
   int64_t ctas = (int64_t)num_sms * ctas_per_sm;
   const int64_t by_rows = (rows + 1) / 2;
   if (by_rows < ctas) ctas = by_rows;
+  if (tiny && a_bytes / 8192 < ctas) ctas = a_bytes / 8192;
+  if (kernel == kKernelAsync && small_plain && ctas > 64) ctas = 64;
   if (ctas < 1) ctas = 1;
   int lpr = 32, ks = 1;
+  if (tiny) {
+    lpr = 32;
+    for (int cand : {4, 8, 16, 32}) {
+      if ((kchunks + cand - 1) / cand <= 4) {
+        lpr = cand;
+        break;
+      }
+    }
+    const int64_t steps = (kchunks + lpr - 1) / lpr;
+    while (2 * ks <= 4 && 2 * ks <= steps) ks *= 2;
+    out->kernel = kKernelDirect;
+    out->lanes_per_row = lpr;
+    out->k_split = ks;
+    out->groups = 1;
+    out->ctas = ctas;
+    out->steps = steps;
+    return true;
+  }
   // permuted scales with plenty of rows: 4 lanes per row, whose 32-row
   // groups read whole 128-byte lines of the scale atoms, and the even K split
   // that leaves about 2 K steps per warp (measured: 4-16% faster than the

@@ -136,12 +136,12 @@ BENCH_SHAPES = [(128, 256, 1), (7168, 2048, 4), (4096, 7168, 8), (7168, 16384, 1
 
 
 @pytest.mark.parametrize("shape,layout,kernel,want", [
-    (BENCH_SHAPES[0], 0, -1, (1, 4, 1, 64, 32)),
+    (BENCH_SHAPES[0], 0, -1, (0, 4, 1, 2, 8)),  # tiny: direct kernel, one CTA per 8 KB of A
     (BENCH_SHAPES[1], 0, -1, (1, 16, 1, 304, 16)),
     (BENCH_SHAPES[2], 0, -1, (1, 16, 1, 304, 16)),
     (BENCH_SHAPES[3], 0, -1, (1, 32, 4, 304, 16)),
     (BENCH_SHAPES[4], 0, -1, (1, 32, 1, 304, 8)),
-    (BENCH_SHAPES[0], 1, -1, (1, 4, 1, 64, 32)),
+    (BENCH_SHAPES[0], 1, -1, (1, 4, 1, 64, 32)),  # permuted: the general schedule
     (BENCH_SHAPES[1], 1, -1, (1, 4, 4, 304, 64)),
     (BENCH_SHAPES[2], 1, -1, (1, 16, 1, 304, 16)),
     (BENCH_SHAPES[3], 1, -1, (1, 16, 8, 304, 32)),
@@ -260,7 +260,10 @@ def test_gemv_ex_option_validation(lib):
 
 def test_kernel_choice(lib):
     assert nv.nvfp4_gemv_plan(100, 0, 3, 0, 152, 2)["kernel"] == nv.KERNEL_DIRECT
-    assert nv.nvfp4_gemv_plan(100, 64, 3, 0, 152, 2)["kernel"] == nv.KERNEL_PIPELINED
+    # up to 512 KB of A the direct kernel; above it the pipelined kernel
+    assert nv.nvfp4_gemv_plan(100, 64, 3, 0, 152, 2)["kernel"] == nv.KERNEL_DIRECT
+    assert nv.nvfp4_gemv_plan(1024, 1024, 1, 0, 152, 2)["kernel"] == nv.KERNEL_DIRECT
+    assert nv.nvfp4_gemv_plan(1025, 1024, 1, 0, 152, 2)["kernel"] == nv.KERNEL_PIPELINED
     with pytest.raises(nv.Nvfp4Error) as e:
         nv.nvfp4_gemv_plan(100, 0, 3, 0, 152, 2, kernel=nv.KERNEL_PIPELINED)
     assert e.value.status == nv.ERR_UNSUPPORTED_SHAPE
@@ -277,7 +280,13 @@ def test_plan_invariants_on_random_shapes(lib):
         sms = int(rng.integers(1, 200))
         plan = nv.nvfp4_gemv_plan(M, K, L, 0, sms, 2)
         kch = K // 64
-        assert plan["kernel"] == (nv.KERNEL_PIPELINED if kch else nv.KERNEL_DIRECT)
+        tiny = M * L * (K // 2) <= 512 << 10
+        assert plan["kernel"] == (nv.KERNEL_PIPELINED if kch and not tiny else nv.KERNEL_DIRECT)
+        if kch and tiny:  # narrow rows, at most 4 K steps split over warps, 8 KB of A per CTA
+            assert plan["steps"] <= 4 or plan["lanes_per_row"] == 32
+            assert plan["ctas"] <= max(1, M * L * (K // 2) // 8192)
+        if kch and not tiny and M * L * (K // 2) <= 2 << 20:
+            assert plan["ctas"] <= 64
         assert plan["lanes_per_row"] in (4, 8, 16, 32) and plan["k_split"] in (1, 2, 4, 8)
         assert plan["steps"] * plan["lanes_per_row"] >= kch
         assert (plan["steps"] - 1) * plan["lanes_per_row"] < max(kch, 1)
