@@ -172,13 +172,19 @@ def gpu_id_for_smi(torch, dev_index: int) -> str:
 # helpers
 # ---------------------------------------------------------------------------
 
+# The files of the CUDA-core GEMV kernels' code: everything under csrc/ but the
+# separate scale-repack and tensor-core kernels and the host planner (whose
+# choice is checked through the recorded schedule instead).
+_NOT_KERNEL_CODE = ("repack.cu", "gemv_tc.cu", "api.cu")
+_SCHEDULE_KEYS = ("kernel", "lanes_per_row", "k_split", "ctas")
+
+
 def kernel_source_hash() -> str:
-    """Hash of the sources the default GEMV launch is built from: every file under
-    csrc/ except the separate scale-repack and tensor-core kernels."""
+    """Hash of the CUDA-core GEMV kernels' sources."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_block_scaled_gemv_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name in ("repack.cu", "gemv_tc.cu"):
+        if name in _NOT_KERNEL_CODE:
             continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
@@ -194,9 +200,10 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def profiled_traffic(workload: str, layout: str):
-    """Per-launch DRAM bytes from the committed ncu summary, if the kernel
-    sources are unchanged since it was captured."""
+def profiled_traffic(workload: str, layout: str, schedule: dict):
+    """Per-launch DRAM bytes from the committed ncu summary, if the kernels'
+    sources are unchanged since it was captured and the launch runs the
+    schedule that was captured (a launch's traffic depends on both)."""
     path = os.path.join(ROOT, "profiles", "gemv_traffic.json")
     if not os.path.exists(path):
         return None
@@ -204,6 +211,9 @@ def profiled_traffic(workload: str, layout: str):
         d = json.load(f)
     entry = d.get(f"{workload}/{layout}")
     if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    captured = entry.get("schedule") or {}
+    if any(captured.get(k) != schedule.get(k) for k in _SCHEDULE_KEYS):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -459,7 +469,7 @@ def run_native(args):
         "single_call_l2_flushed_us": {"median": round(single_med, 3), "min": round(single_min, 3)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": profiled_traffic(name, args.layout),
+                     "traffic": profiled_traffic(name, args.layout, plan),
                      "peak_source": peaks["source"]},
         "cpu_baseline": {"value": round(cpu_us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": cpu_sample},

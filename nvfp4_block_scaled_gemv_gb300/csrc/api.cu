@@ -207,7 +207,9 @@ void tc_rule(int64_t M, int64_t N, int64_t K, int64_t L, int64_t slots, int* sta
 // GB300: 177 us against 182-190 us on M16384_K8192_L16 (1.07 GB of A), level
 // on M4096_K7168_L8 (117 MB), slower below.
 bool tensor_gemv_pays(int64_t M, int64_t K, int64_t L, bool permuted) {
-  return permuted && K > 0 && M * L * (K / 2) >= (int64_t(1) << 29);
+  // (the kernel indexes tiles and batches with 32-bit TMA coordinates)
+  return permuted && K > 0 && M * L * (K / 2) >= (int64_t(1) << 29) &&
+         L * ((M + 127) / 128) <= 0x7fffffff;
 }
 
 // The rule above with the CTAs of the 2-stage kernel resident on this device.

@@ -174,6 +174,9 @@ def test_tensor_kernel_plans(lib):
     assert nv.nvfp4_gemv_plan(16384, 8192, 16, 0, 152, 2)["kernel"] == nv.KERNEL_PIPELINED
     assert nv.nvfp4_gemv_plan(16384, 8192, 2, 1, 152, 2)["kernel"] == nv.KERNEL_PIPELINED
     assert nv.nvfp4_gemv_plan(16384, 8192, 8, 1, 152, 2)["kernel"] == nv.KERNEL_TENSOR
+    # more tiles than 32-bit tile coordinates hold: the pipelined kernel
+    assert nv.nvfp4_gemv_plan(1, 1024, 1 << 31, 1, 152, 2)["kernel"] == nv.KERNEL_PIPELINED
+    assert nv.nvfp4_gemv_plan(1, 1024, (1 << 31) - 1, 1, 152, 2)["kernel"] == nv.KERNEL_TENSOR
     rng = np.random.default_rng(1)
     for _ in range(200):
         M, K, L = int(rng.integers(1, 30000)), 64 * int(rng.integers(1, 400)), int(rng.integers(1, 9))
