@@ -81,12 +81,15 @@ typedef enum {
  * (pointers may be NULL).  K == 0 writes +0 to every c (a, b, sfa, sfb may be
  * NULL).  Limits: K <= 2^30, M*L < 2^40.
  * Alignment: a, b, sfa, sfb 32-byte aligned; c 2-byte aligned.
- * Accuracy: each 16-element block's dot product is exact; blocks are scaled
- * and summed in FP32; c is rounded to nearest even (overflow gives +-Inf;
- * a NaN scale gives NaN).  Results are bitwise reproducible run to run.  The
- * FP32 summation order follows the launch schedule, which the library picks
- * per shape and scale layout; under one schedule (nvfp4_gemv_explicit) the
- * two layouts give identical bits.
+ * Accuracy: on the CUDA-core kernels each 16-element block's dot product is
+ * exact and blocks are scaled and summed in FP32; the tensor-core kernel
+ * (pre-permuted scales with at least 512 MB of A) sums in the MMA's FP32 order.
+ * c is rounded to nearest even (overflow gives +-Inf; a NaN scale gives NaN)
+ * and stays within 1e-3 * sum|terms| + 1 fp16 ulp of the exact result.
+ * Results are bitwise reproducible run to run.  The FP32 summation order
+ * follows the launch schedule, which the library picks per shape and scale
+ * layout; under one CUDA-core schedule (nvfp4_gemv_explicit) the two layouts
+ * give identical bits.
  * Execution detail: before waiting for the preceding work on the stream, the
  * kernel may ask the L2 to prefetch lines of a (a hint that returns no data;
  * every input is read only after that work has completed).
@@ -255,17 +258,24 @@ int nvfp4_tensor_wait_timeouts(int reset);
  * inspection and tests.  kernel = -1 gives the plan nvfp4_gemv uses, an
  * nvfp4_kernel_t value that kernel's plan (NVFP4_ERR_UNSUPPORTED_SHAPE if it
  * cannot run the shape).  num_sms is the device's multiprocessor count and
- * ctas_per_sm the number of the kernel's CTAs resident per SM (pass 0 to use
- * the compiled-in default of 2).
+ * ctas_per_sm the number of the CUDA-core kernel's CTAs resident per SM (pass
+ * 0 to use the compiled-in default of 2).  nvfp4_gemv picks: the tensor-core
+ * kernel for pre-permuted scales with at least 512 MB of A; the direct kernel
+ * for K = 0 and for plain scales up to 512 KB of A; the pipelined kernel
+ * otherwise.  For the tensor-core kernel the plan assumes 4 resident CTAs per
+ * SM; a launch recomputes its grid from the device's limits.
  */
 typedef struct {
   int kernel;         /* nvfp4_kernel_t */
-  int lanes_per_row;  /* lanes of a warp that share one row (32-byte K chunk each) */
-  int k_split;        /* warps of a CTA that split one row's K range */
-  int rows_per_pass;  /* rows a warp reduces at once */
+  int lanes_per_row;  /* lanes of a warp that share one row (32-byte K chunk
+                         each); tensor-core kernel: pipeline stages per CTA */
+  int k_split;        /* warps of a CTA that split one row's K range;
+                         tensor-core kernel: CTAs per cluster */
+  int rows_per_pass;  /* rows a warp reduces at once; tensor-core kernel: 128 */
   int threads_per_cta;
   int64_t ctas;       /* grid size */
-  int64_t steps;      /* K chunks per lane per row, ceil(K/64 / lanes_per_row) */
+  int64_t steps;      /* K chunks per lane per row, ceil(K/64 / lanes_per_row);
+                         tensor-core kernel: 256-element K stages, ceil(K/256) */
 } nvfp4_gemv_plan_t;
 
 nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, int kernel,

@@ -331,7 +331,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ks = cluster_size(), rank = cluster_rank();
   const int cid = (int)(blockIdx.x / ks), nclusters = (int)(gridDim.x / ks);
-  const int ntiles = cid < p.tiles ? (p.tiles - cid + nclusters - 1) / nclusters : 0;
+  // tiles of this cluster: cid, cid + nclusters, ... below p.tiles (< 2^31)
+  const int ntiles =
+      cid < p.tiles ? (int)(((int64_t)p.tiles - cid + nclusters - 1) / nclusters) : 0;
 
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
