@@ -63,7 +63,7 @@ def run_pipeline(stages, stage_counts, seed):
                 st = c * sc + pos
                 while not full[st].done(ph):
                     yield None
-                assert slot_data[st] == (j, i), "a chain read a stale stage"
+                assert slot_data.get(st) == (j, i), "a chain read a stale stage"
                 yield ("mma", st)
                 pos += 1
                 if pos == sc:
