@@ -59,6 +59,7 @@ class Nvfp4Error(RuntimeError):
 KERNEL_DIRECT = 0
 KERNEL_PIPELINED = 1
 KERNEL_TENSOR = 2
+KERNEL_BLOCKDOT = 3
 
 
 class _Plan(ctypes.Structure):

@@ -144,7 +144,9 @@ nvfp4_status_t run_gemv(const void* a, const void* b, const void* sfa, const voi
   const bool permuted = sf_layout == NVFP4_SF_PERMUTED_128x4;
   const GemvParams p = make_params(a, b, sfa, sfb, c, M, K, L, permuted, plan, opt);
   cudaError_t err;
-  if (plan.kernel == kKernelTensor)
+  if (plan.kernel == kKernelBlockDot)
+    err = launch_blockdot(p, permuted, L, plan.lanes_per_row, plan.ctas, stream);
+  else if (plan.kernel == kKernelTensor)
     err = launch_gemv_tc(p, 1, L, K / 2, plan.lanes_per_row, plan.k_split, plan.ctas, stream);
   else if (plan.kernel == kKernelAsync)
     err = permuted ? launch_async_permuted(p, plan, stream) : launch_async_plain(p, plan, stream);
@@ -202,14 +204,31 @@ void tc_rule(int64_t M, int64_t N, int64_t K, int64_t L, int64_t slots, int* sta
   *ctas = (tiles < resident ? tiles : resident) * ks;
 }
 
-// The GEMV (N = 1) on the tensor-core kernel instead of the pipelined
-// CUDA-core kernel: pre-permuted scales and at least 512 MB of A.  Measured on
-// GB300: 177 us against 182-190 us on M16384_K8192_L16 (1.07 GB of A), level
-// on M4096_K7168_L8 (117 MB), slower below.
-bool tensor_gemv_pays(int64_t M, int64_t K, int64_t L, bool permuted) {
-  // (the kernel indexes tiles and batches with 32-bit TMA coordinates)
-  return permuted && K > 0 && M * L * (K / 2) >= (int64_t(1) << 29) &&
-         L * ((M + 127) / 128) <= 0x7fffffff;
+// Shapes the block-dot kernel can run: K > 0; plain scales need K % 256 == 0
+// (their rows of K/16 bytes are TMA boxes, whose row stride must be a multiple
+// of 16 bytes) and a sfb batch stride that keeps 16-byte alignment; batches
+// and rows are 32-bit TMA coordinates.
+bool blockdot_shape_ok(int64_t M, int64_t K, int64_t L, bool permuted) {
+  if (K <= 0 || M < 1 || L < 1 || M > 0x7fffffff || L > 0x7fffffff) return false;
+  return permuted || K % 256 == 0;
+}
+
+// Dynamic shared memory a block-dot CTA may use (one CTA per SM: the 227 KB
+// opt-in limit less the kernel's static barriers).
+constexpr size_t kBlockDotSmemBudget = 232448 - 1024;
+
+// Block-dot schedule: one CTA per SM (no more than the row units), and the
+// deepest ring of K-stage slots that fits.
+void blockdot_rule(int64_t M, int64_t K, int64_t L, bool permuted, int num_sms, int* stages,
+                   int64_t* ctas) {
+  const int64_t ur = blockdot_unit_rows(permuted);
+  const int64_t units = L * ((M + ur - 1) / ur);
+  int64_t n = num_sms;
+  if (units < n) n = units;
+  if (n < 1) n = 1;
+  *ctas = n;
+  *stages = blockdot_max_stages(permuted, blockdot_column_blocks(K),
+                                blockdot_slot_rows(M, L, permuted, n), kBlockDotSmemBudget);
 }
 
 // The rule above with the CTAs of the 2-stage kernel resident on this device.
@@ -266,7 +285,7 @@ nvfp4_status_t run_gemm_tc(const void* a, const void* b, const void* sfa, const 
 }  // namespace
 
 int rows_per_pass(const GemvPlan& plan) {
-  if (plan.kernel == kKernelTensor) return 128;  // one tile of A rows
+  if (plan.kernel == kKernelTensor || plan.kernel == kKernelBlockDot) return 128;  // a tile of A rows
   return plan.kernel == kKernelAsync ? kAsyncItems * (32 / plan.lanes_per_row) * plan.groups
                                      : kRowsPerPass;
 }
@@ -348,7 +367,7 @@ int async_groups(int64_t M, int64_t L, bool permuted, int lanes_per_row, int k_s
 bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int num_sms,
                int ctas_per_sm, GemvPlan* out) {
   if (M < 0 || K < 0 || L < 0 || num_sms < 1 || ctas_per_sm < 1 || out == nullptr) return false;
-  if (kernel < -1 || kernel > kKernelTensor) return false;
+  if (kernel < -1 || kernel > kKernelBlockDot) return false;
   const int64_t kchunks = K / 64;
   const int64_t a_bytes = M * L * (K / 2);
   // Tiny problems with plain scales (measured on GB300 over 16 KB .. 2 MB of
@@ -360,10 +379,23 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
   // the general schedule: the same rule was slower for some of them.)
   const bool small_plain = !permuted && kchunks > 0 && a_bytes <= (int64_t(2) << 20);
   const bool tiny = kernel == -1 && small_plain && a_bytes <= (int64_t(512) << 10);
-  if (kernel == -1)
-    kernel = tensor_gemv_pays(M, K, L, permuted) ? kKernelTensor
-             : tiny || kchunks == 0              ? kKernelDirect
-                                                 : kKernelAsync;
+  // (the block-dot and tensor-core kernels are selected explicitly: measured
+  // on GB300, the pipelined kernel is as fast or faster on every workload)
+  if (kernel == -1) kernel = tiny || kchunks == 0 ? kKernelDirect : kKernelAsync;
+  if (kernel == kKernelBlockDot) {
+    if (!blockdot_shape_ok(M, K, L, permuted)) return false;
+    int stages = 2;
+    int64_t ctas = 1;
+    blockdot_rule(M, K, L, permuted, num_sms, &stages, &ctas);
+    out->kernel = kKernelBlockDot;
+    out->lanes_per_row = stages;
+    out->k_split = 1;
+    out->groups = 1;
+    out->ctas = ctas;
+    const int64_t stage_chunks = 4 * blockdot_column_blocks(K);  // 64-element chunks per stage
+    out->steps = (kchunks + stage_chunks - 1) / stage_chunks;
+    return true;
+  }
   if (kernel == kKernelTensor) {
     if (!permuted || kchunks == 0) return false;
     // host-only estimate: 4 CTAs of the 2-stage kernel resident per SM
@@ -484,17 +516,8 @@ nvfp4_status_t nvfp4_gemv_ex(const void* a, const void* b, const void* sfa, cons
   cudaError_t err = device_info(&sms, &occ, nullptr);
   if (err != cudaSuccess) return cuda_failure(err);
   GemvPlan plan;
-  if (!plan_gemv(M, K, L, sf_layout == NVFP4_SF_PERMUTED_128x4, -1, sms, occ, &plan))
-    return NVFP4_ERR_INVALID_VALUE;
-  if (plan.kernel == kKernelTensor) {
-    int stages = 2, ks = 1;
-    int64_t ctas = 1;
-    err = plan_tc(M, 1, K, L, &stages, &ks, &ctas);
-    if (err != cudaSuccess) return cuda_failure(err);
-    plan.lanes_per_row = stages;
-    plan.k_split = ks;
-    plan.ctas = ctas;
-  }
+  const bool permuted = sf_layout == NVFP4_SF_PERMUTED_128x4;
+  if (!plan_gemv(M, K, L, permuted, -1, sms, occ, &plan)) return NVFP4_ERR_INVALID_VALUE;
   return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, opt, (cudaStream_t)stream);
 }
 
@@ -504,8 +527,33 @@ nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa
                                    int64_t ctas, struct CUstream_st* stream) {
   nvfp4_status_t st = validate_gemv_shape(M, K, L, sf_layout);
   if (st != NVFP4_OK) return st;
-  if (kernel != kKernelDirect && kernel != kKernelAsync && kernel != kKernelTensor)
+  if (kernel != kKernelDirect && kernel != kKernelAsync && kernel != kKernelTensor &&
+      kernel != kKernelBlockDot)
     return NVFP4_ERR_INVALID_VALUE;
+  const bool permuted = sf_layout == NVFP4_SF_PERMUTED_128x4;
+  if (kernel == kKernelBlockDot) {
+    // lanes_per_row = ring slots (0: the most that fit), k_split 1
+    if (k_split != 1 || ctas < 1 || ctas > 0x7fffffff || lanes_per_row < 0 ||
+        lanes_per_row == 1 || lanes_per_row > kBlockDotMaxStages)
+      return NVFP4_ERR_INVALID_VALUE;
+    if (!blockdot_shape_ok(M < 1 ? 1 : M, K, L < 1 ? 1 : L, permuted)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || L == 0) return NVFP4_OK;
+    st = validate_gemv_pointers(a, b, sfa, sfb, c, K);
+    if (st != NVFP4_OK) return st;
+    const int slot_rows = blockdot_slot_rows(M, L, permuted, ctas);
+    const int most = blockdot_max_stages(permuted, blockdot_column_blocks(K), slot_rows,
+                                         kBlockDotSmemBudget);
+    if (lanes_per_row > most) return NVFP4_ERR_INVALID_VALUE;
+    GemvPlan plan;
+    plan.kernel = kKernelBlockDot;
+    plan.lanes_per_row = lanes_per_row == 0 ? most : lanes_per_row;
+    plan.k_split = 1;
+    plan.groups = 1;
+    plan.ctas = ctas;
+    plan.steps = (K + 255) / 256;
+    return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, kDefaultOptions,
+                    (cudaStream_t)stream);
+  }
   // lanes per row; for the tensor-core kernel, pipeline stages per CTA
   if (kernel == kKernelTensor ? (lanes_per_row != 2 && lanes_per_row != 4)
                               : (lanes_per_row != 4 && lanes_per_row != 8 &&
@@ -622,14 +670,15 @@ nvfp4_status_t nvfp4_gemm_small_n_plan(int64_t M, int64_t N, int64_t K, int64_t 
 int nvfp4_last_cuda_error(void) { return g_last_cuda_error; }
 
 int nvfp4_tensor_wait_timeouts(int reset) {
-  int v = 0;
-  const cudaError_t err = tc_wait_timeouts(reset, &v);
+  int v = 0, w = 0;
+  cudaError_t err = tc_wait_timeouts(reset, &v);
+  if (err == cudaSuccess) err = blockdot_wait_timeouts(reset, &w);
   if (err != cudaSuccess) {
     g_last_cuda_error = (int)err;
     (void)cudaGetLastError();
     return -1;
   }
-  return v;
+  return v + w;
 }
 
 nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, int kernel,
@@ -638,7 +687,7 @@ nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, i
   nvfp4_status_t st = validate_gemv_shape(M, K, L, sf_layout);
   if (st != NVFP4_OK) return st;
   GemvPlan plan;
-  if (kernel < -1 || kernel > kKernelTensor) return NVFP4_ERR_INVALID_VALUE;
+  if (kernel < -1 || kernel > kKernelBlockDot) return NVFP4_ERR_INVALID_VALUE;
   if (!plan_gemv(M, K, L, sf_layout == NVFP4_SF_PERMUTED_128x4, kernel, num_sms,
                  ctas_per_sm > 0 ? ctas_per_sm : kGemvMinCtasPerSm, &plan))
     return NVFP4_ERR_UNSUPPORTED_SHAPE;
@@ -646,7 +695,9 @@ nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, i
   out->lanes_per_row = plan.lanes_per_row;
   out->k_split = plan.k_split;
   out->rows_per_pass = rows_per_pass(plan);
-  out->threads_per_cta = plan.kernel == kKernelTensor ? kTcThreadsPerCta : kGemvThreads;
+  out->threads_per_cta = plan.kernel == kKernelTensor     ? kTcThreadsPerCta
+                         : plan.kernel == kKernelBlockDot ? kBlockDotThreads
+                                                          : kGemvThreads;
   out->ctas = plan.ctas;
   out->steps = plan.steps;
   return NVFP4_OK;

@@ -45,13 +45,10 @@
 #include <cstdint>
 #include <cstring>
 
-#include <cuda.h>  // CUtensorMap (the type only; the encoder is looked up at run time)
-#include <cudaTypedefs.h>
-
 #include <cuda_fp16.h>
 
 #include "internal.h"
-#include "ptx.cuh"
+#include "tc_ptx.cuh"
 
 namespace nvfp4 {
 
@@ -63,7 +60,6 @@ constexpr int kTcThreads = kTcThreadsPerCta;  // 7 warps
 constexpr uint32_t kTcABytes = 128 * 128;   // 128 rows x 256 elements
 constexpr uint32_t kTcBBytes = 16 * 128;    // 16 rows x 256 elements (rows 0..N-1 = b)
 constexpr uint32_t kTcSfBytes = 4 * 512;    // 4 scale atoms (K = 256)
-constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s
 
 // TMEM columns a CTA allocates: accumulators [2 chains][2][16], then sfa and
 // sfb [stage][4 atoms][4 columns] each (a power of two, at least 32).
@@ -82,10 +78,8 @@ static_assert(3 * (tc_smem_bytes(4, 1) + 1024) > 228 * 1024, "at most 2 CTAs of 
 static_assert((tc_smem_bytes(4, 1) + 1024) + 3 * (tc_smem_bytes(2, 1) + 1024) > 228 * 1024,
               "at most 2 CTAs of 2 stages beside one of 4");
 
-// Instruction descriptor of the block-scaled MMA: A and B E2M1 (format 1),
-// both K-major, N = 16 (N/8 at bit 17), UE4M3 scales (bit 23 clear),
-// M = 128 (M/16 at bit 24), scale ids 0, dense K = 64.
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+// Instruction descriptor: N = 16 rows of B (see tc::mxf4nvf4_idesc).
+constexpr uint32_t kIdesc = tc::mxf4nvf4_idesc(16);
 
 struct TcParams {
   CUtensorMap tmap_a;  // uint8 {K/2, M, L}, box {128, 128, 1}, 128-byte swizzle
@@ -106,194 +100,6 @@ __device__ __forceinline__ uint16_t finish_output_tc(float alpha, const uint16_t
                                                      int64_t idx) {
   const float o = bias ? fmaf(v, alpha, __half2float(__ushort_as_half(bias[idx]))) : v * alpha;
   return __half_as_ushort(__float2half_rn(o));
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// Acquire at cluster scope: the phase was completed by arrivals from other
-// CTAs of the cluster whose prior shared-memory stores must be visible.
-__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;"
-      "\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// Bounded wait for the phase of the given parity; false (and ok cleared, one
-// timeout counted) if it did not complete within kWaitNs, or if ok was
-// already clear.
-template <bool CLUSTER>
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, bool& ok) {
-  if (!ok) return false;
-  if (CLUSTER ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (CLUSTER ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
-    if ((i & 255u) == 0 && global_ns() - t0 > kWaitNs) {
-      atomicAdd(&g_tc_timeouts, 1);
-      ok = false;
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-// The same shared-memory offset in the CTA of the given cluster rank.
-__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-__device__ __forceinline__ float ld_remote_f32(uint32_t cluster_addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-               ::: "memory");
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            int z, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
-      "[%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// Shared-memory matrix descriptors (64-bit): start address >> 4 in bits
-// 0-13, leading byte offset >> 4 in 16-29, stride byte offset >> 4 in
-// 32-45, descriptor version 1 in 46-47, layout in 61-63.
-// K-major operand tile in the 128-byte swizzled layout the TMA writes: rows
-// of 128 bytes, 8-row groups 1024 bytes apart; the K step inside the swizzle
-// span moves the start address by 32 bytes.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-// A scale atom as the 32 x 128-bit copy source: 32 rows of 16 bytes, no
-// swizzle, 8-row core matrices 128 bytes apart.
-__device__ __forceinline__ uint64_t desc_atom(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_copy_atom(uint32_t taddr, uint64_t desc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
-               : "memory");
-}
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t sfa,
-                                       uint32_t sfb, bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], "
-      "[%6], p;\n\t}" ::"r"(d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"((uint32_t)accumulate), "r"(sfa), "r"(sfb)
-      : "memory");
-}
-// Columns 0..NC-1 of this warp's 32 TMEM lanes (lane i of the warp gets
-// row 32*quarter + i), as fp32.
-template <int NC>
-__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&out)[NC]) {
-  uint32_t v[NC];
-  if constexpr (NC == 1) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v[0]) : "r"(taddr));
-  } else if constexpr (NC == 2) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
-                 : "=r"(v[0]), "=r"(v[1])
-                 : "r"(taddr));
-  } else if constexpr (NC == 4) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
-                 : "r"(taddr));
-  } else if constexpr (NC == 8) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
-                   "=r"(v[6]), "=r"(v[7])
-                 : "r"(taddr));
-  } else {
-    static_assert(NC == 16, "NC in {1, 2, 4, 8, 16}");
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-          "=r"(v[14]), "=r"(v[15])
-        : "r"(taddr));
-  }
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int n = 0; n < NC; ++n) out[n] = __uint_as_float(v[n]);
-}
-
-// Arrive on the mbarrier once every tcgen05 operation this thread issued so
-// far has completed.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
 }
 
 // S: pipeline stages per CTA (2 or 4; fewer stages let more CTAs share an SM,
@@ -329,7 +135,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   static_assert(S % 2 == 0, "two chains of equal rings");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t ks = cluster_size(), rank = cluster_rank();
+  const uint32_t ks = tc::cluster_size(), rank = tc::cluster_rank();
   const int cid = (int)(blockIdx.x / ks), nclusters = (int)(gridDim.x / ks);
   // tiles of this cluster: cid, cid + nclusters, ... below p.tiles (< 2^31)
   const int ntiles =
@@ -338,16 +144,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int st = 0; st < S; ++st) {
-      mbar_init(full_bar(st), 1);
-      mbar_init(empty_bar(st), 1);
+      tc::mbar_init(full_bar(st), 1);
+      tc::mbar_init(empty_bar(st), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(dfull_bar + 8u * i, 2);  // one commit per MMA chain
-      mbar_init(dempty_bar + 8u * i, 128);
-      mbar_init(rfull_bar + 8u * i, ks > 1 ? (ks - 1) * 128 : 1);
-      mbar_init(rfree_bar + 8u * i, 128);
+      tc::mbar_init(dfull_bar + 8u * i, 2);  // one commit per MMA chain
+      tc::mbar_init(dempty_bar + 8u * i, 128);
+      tc::mbar_init(rfull_bar + 8u * i, ks > 1 ? (ks - 1) * 128 : 1);
+      tc::mbar_init(rfree_bar + 8u * i, 128);
     }
-    mbar_init(drain_bar, 2);
+    tc::mbar_init(drain_bar, 2);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   // rows N..15 of every B stage start as zeros and are never written again
@@ -363,10 +169,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  tc_fence_before();
+  tc::fence_before();
   __syncthreads();
-  cluster_sync();  // every CTA's barriers are initialised before any remote arrive
-  tc_fence_after();
+  tc::cluster_sync();  // every CTA's barriers are initialised before any remote arrive
+  tc::fence_after();
   const uint32_t tmem = tmem_slot;
   bool ok = true;
 
@@ -387,7 +193,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         stage_range(cid, s0, cnt);
         const int l = cid / p.rest_m, mt = cid % p.rest_m;
         for (int i = 0; i < cnt && i < 2 * S; ++i)
-          tma_prefetch_3d(&p.tmap_a, (s0 + i) * 128, mt * 128, l);
+          tc::tma_prefetch_3d(&p.tmap_a, (s0 + i) * 128, mt * 128, l);
       }
       pdl_wait();
       // stage i of a tile goes to MMA chain i % 2, through that chain's ring
@@ -402,15 +208,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int s = s0 + i;
           const int nk = min(4, p.rest_k - 4 * s);
           const int c = i & 1, st = c * SC + pos[c];
-          if (mbar_wait<false>(empty_bar(st), ph[c] ^ 1u, ok)) {
+          if (tc::mbar_wait<false>(empty_bar(st), ph[c] ^ 1u, ok, &g_tc_timeouts)) {
             const uint32_t fb = full_bar(st);
-            mbar_expect_tx(fb, kTcABytes + 128u * (uint32_t)p.N + 2u * (uint32_t)nk * 512u);
-            tma_load_3d(a_s + st * kTcABytes, &p.tmap_a, s * 128, mt * 128, l, fb);
-            tma_load_3d(b_s + st * kTcBBytes, &p.tmap_b, s * 128, 0, l, fb);
-            bulk_load(sfa_s + st * kTcSfBytes,
+            tc::mbar_expect_tx(fb, kTcABytes + 128u * (uint32_t)p.N + 2u * (uint32_t)nk * 512u);
+            tc::tma_load_3d(a_s + st * kTcABytes, &p.tmap_a, s * 128, mt * 128, l, fb);
+            tc::tma_load_3d(b_s + st * kTcBBytes, &p.tmap_b, s * 128, 0, l, fb);
+            tc::bulk_load(sfa_s + st * kTcSfBytes,
                       p.sfa + (((int64_t)l * p.rest_m + mt) * p.rest_k + 4 * s) * 512,
                       (uint32_t)nk * 512u, fb);
-            bulk_load(sfb_s + st * kTcSfBytes, p.sfb + (int64_t)l * p.sfb_stride + (int64_t)s * 2048,
+            tc::bulk_load(sfb_s + st * kTcSfBytes, p.sfb + (int64_t)l * p.sfb_stride + (int64_t)s * 2048,
                       (uint32_t)nk * 512u, fb);
             ++issued[c];
           }
@@ -426,7 +232,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int c = 0; c < 2; ++c)
         for (int k = 0; k < SC && k < issued[c]; ++k) {
           const int i_last = issued[c] - 1 - k;
-          mbar_wait<false>(full_bar(c * SC + i_last % SC), (uint32_t)((i_last / SC) & 1), drain_ok);
+          tc::mbar_wait<false>(full_bar(c * SC + i_last % SC), (uint32_t)((i_last / SC) & 1), drain_ok, &g_tc_timeouts);
         }
     } else {
       pdl_wait();
@@ -441,7 +247,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int j = 0; j < ntiles; ++j) {
       const int acc = j & 1;
       const uint32_t d = tmem + (uint32_t)(16 * (2 * c + acc));
-      if (lane == 0) mbar_wait<false>(dempty_bar + 8u * acc, ((uint32_t)(j >> 1) & 1u) ^ 1u, ok);
+      if (lane == 0) tc::mbar_wait<false>(dempty_bar + 8u * acc, ((uint32_t)(j >> 1) & 1u) ^ 1u, ok, &g_tc_timeouts);
       int s0, cnt;
       stage_range(cid + j * nclusters, s0, cnt);
       bool first = true;
@@ -449,20 +255,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int s = s0 + i;
         const int nk = min(4, p.rest_k - 4 * s);
         const int st = c * SC + pos;
-        if (lane == 0 && mbar_wait<false>(full_bar(st), ph, ok)) {
-          tc_fence_after();
+        if (lane == 0 && tc::mbar_wait<false>(full_bar(st), ph, ok, &g_tc_timeouts)) {
+          tc::fence_after();
           for (int kk = 0; kk < nk; ++kk) {
-            tc_copy_atom(tmem + kSfaCol + (uint32_t)(16 * st + 4 * kk),
-                         desc_atom(sfa_s + st * kTcSfBytes + 512u * kk));
-            tc_copy_atom(tmem + kSfbCol + (uint32_t)(16 * st + 4 * kk),
-                         desc_atom(sfb_s + st * kTcSfBytes + 512u * kk));
+            tc::copy_atom(tmem + kSfaCol + (uint32_t)(16 * st + 4 * kk),
+                         tc::desc_atom(sfa_s + st * kTcSfBytes + 512u * kk));
+            tc::copy_atom(tmem + kSfbCol + (uint32_t)(16 * st + 4 * kk),
+                         tc::desc_atom(sfb_s + st * kTcSfBytes + 512u * kk));
           }
           for (int kk = 0; kk < nk; ++kk)
-            tc_mma(d, desc_sw128(a_s + st * kTcABytes + 32u * kk),
-                   desc_sw128(b_s + st * kTcBBytes + 32u * kk),
+            tc::mma(d, tc::desc_sw128(a_s + st * kTcABytes + 32u * kk),
+                    tc::desc_sw128(b_s + st * kTcBBytes + 32u * kk), kIdesc,
                    tmem + kSfaCol + (uint32_t)(16 * st + 4 * kk),
                    tmem + kSfbCol + (uint32_t)(16 * st + 4 * kk), !first || kk > 0);
-          tc_commit(empty_bar(st));
+          tc::commit(empty_bar(st));
         }
         first = false;
         if (++pos == SC) {
@@ -472,13 +278,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // a chain with no stage in this tile commits at once (its accumulator is
       // not read)
-      if (lane == 0 && ok) tc_commit(dfull_bar + 8u * acc);
+      if (lane == 0 && ok) tc::commit(dfull_bar + 8u * acc);
     }
     if (lane == 0) {
       // every MMA and TMEM copy of this chain has finished before TMEM is released
-      tc_commit(drain_bar);
+      tc::commit(drain_bar);
       bool drain_ok = true;
-      mbar_wait<false>(drain_bar, 0, drain_ok);
+      tc::mbar_wait<false>(drain_bar, 0, drain_ok, &g_tc_timeouts);
     }
     __syncwarp();
   } else {
@@ -490,7 +296,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int t = cid + j * nclusters;
       const int l = t / p.rest_m, mt = t % p.rest_m;
       const int acc = j & 1;
-      mbar_wait<false>(dfull_bar + 8u * acc, (uint32_t)(j >> 1) & 1u, ok);
+      tc::mbar_wait<false>(dfull_bar + 8u * acc, (uint32_t)(j >> 1) & 1u, ok, &g_tc_timeouts);
       ok = __all_sync(0xffffffffu, ok);  // the TMEM load below is warp-collective
       float part[NC];
 #pragma unroll
@@ -498,36 +304,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int s0, cnt;
       stage_range(t, s0, cnt);
       if (ok && cnt > 0) {  // K = 0: the sums are zero and no MMA ran
-        tc_fence_after();
-        tmem_load_cols<NC>(tmem + (uint32_t)(16 * acc) + ((32u * q) << 16), part);
+        tc::fence_after();
+        tc::tmem_load_cols<NC>(tmem + (uint32_t)(16 * acc) + ((32u * q) << 16), part);
         if (cnt > 1) {  // chain 1 took the odd stages
           float odd[NC];
-          tmem_load_cols<NC>(tmem + (uint32_t)(16 * (2 + acc)) + ((32u * q) << 16), odd);
+          tc::tmem_load_cols<NC>(tmem + (uint32_t)(16 * (2 + acc)) + ((32u * q) << 16), odd);
 #pragma unroll
           for (int n = 0; n < NC; ++n) part[n] += odd[n];
         }
       }
-      tc_fence_before();
-      mbar_arrive(dempty_bar + 8u * acc);
+      tc::fence_before();
+      tc::mbar_arrive(dempty_bar + 8u * acc);
       const int64_t m = (int64_t)mt * 128 + r;
       const int buf = j & 1;
       const uint32_t use = (uint32_t)(j >> 1);
       if (ks > 1 && rank != 0) {
         // wait until rank 0 has read this buffer's previous use, then publish
-        mbar_wait<true>(rfree_bar + 8u * buf, (use & 1u) ^ 1u, ok);
+        tc::mbar_wait<true>(rfree_bar + 8u * buf, (use & 1u) ^ 1u, ok, &g_tc_timeouts);
 #pragma unroll
         for (int n = 0; n < NC; ++n) red[(buf * NC + n) * 128 + r] = part[n];
-        mbar_arrive_remote(map_rank(rfull_bar + 8u * buf, 0));
+        tc::mbar_arrive_remote(tc::map_rank(rfull_bar + 8u * buf, 0));
         continue;
       }
       if (ks > 1) {
-        const bool got = mbar_wait<true>(rfull_bar + 8u * buf, use & 1u, ok);
+        const bool got = tc::mbar_wait<true>(rfull_bar + 8u * buf, use & 1u, ok, &g_tc_timeouts);
         for (uint32_t k = 1; k < ks; ++k) {
 #pragma unroll
           for (int n = 0; n < NC; ++n)
-            if (got) part[n] += ld_remote_f32(map_rank(red_s + 4u * (uint32_t)((buf * NC + n) * 128 + r), k));
+            if (got) part[n] += tc::ld_remote_f32(tc::map_rank(red_s + 4u * (uint32_t)((buf * NC + n) * 128 + r), k));
         }
-        for (uint32_t k = 1; k < ks; ++k) mbar_arrive_remote(map_rank(rfree_bar + 8u * buf, k));
+        for (uint32_t k = 1; k < ks; ++k) tc::mbar_arrive_remote(tc::map_rank(rfree_bar + 8u * buf, k));
       }
       if (ok && m < p.M) {
 #pragma unroll
@@ -541,19 +347,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
 
-  tc_fence_before();
+  tc::fence_before();
   __syncthreads();
-  cluster_sync();  // no peer still reads or signals this CTA's shared memory
+  tc::cluster_sync();  // no peer still reads or signals this CTA's shared memory
   if (warp == 1) {
-    tc_fence_after();
+    tc::fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
                  : "memory");
   }
 }
 
-// cuTensorMapEncodeTiled, looked up once through the runtime (no link
-// against the driver library).
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* f = nullptr;
@@ -566,6 +372,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   }();
   return fn;
 }
+
+namespace {
 
 using TcKernel = void (*)(TcParams);
 

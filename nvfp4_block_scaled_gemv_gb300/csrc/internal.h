@@ -19,7 +19,7 @@ constexpr int kAsyncStages = 3;
 constexpr int kAsyncStageBytes = kAsyncItems * (32 * 32 + 32 * 4);
 constexpr int kAsyncSmemBytes = kGemvWarps * kAsyncStages * kAsyncStageBytes;
 
-enum KernelKind { kKernelDirect = 0, kKernelAsync = 1, kKernelTensor = 2 };
+enum KernelKind { kKernelDirect = 0, kKernelAsync = 1, kKernelTensor = 2, kKernelBlockDot = 3 };
 
 // Everything a GEMV kernel needs, by value (kernel parameter space).
 struct GemvParams {
@@ -89,6 +89,26 @@ cudaError_t tc_max_active_clusters(int stages, int64_t N, int ks, int* out);
 // Bounded waits of the tensor-core kernel that gave up (read, then optionally
 // cleared; synchronous).
 cudaError_t tc_wait_timeouts(int reset, int* out);
+
+// Block-dot kernel (gemv_blockdot.cu): tensor-core 16-element block dots
+// (selector scales), E4M3 scales applied on the CUDA cores.  One CTA of
+// kBlockDotThreads threads per SM, a ring of `stages` (2..kBlockDotMaxStages)
+// K-stage slots of slot_rows rows and blockdot_column_blocks(K) 128-byte
+// column blocks; rows handed out in units of blockdot_unit_rows() (8) rows.
+// Needs K > 0; plain scales also K % 256 == 0.
+constexpr int kBlockDotThreads = 192;
+constexpr int kBlockDotMaxStages = 32;
+int blockdot_unit_rows(bool permuted);
+// 128-byte column blocks per K stage: 2 when K % 256 == 0, else 1.
+int blockdot_column_blocks(int64_t K);
+// Rows of a ring slot for a launch over `ctas` CTAs (the longest tile).
+int blockdot_slot_rows(int64_t M, int64_t L, bool permuted, int64_t ctas);
+size_t blockdot_smem_bytes(bool permuted, int column_blocks, int slot_rows, int stages);
+// Most ring slots that fit smem_per_cta bytes of dynamic shared memory.
+int blockdot_max_stages(bool permuted, int column_blocks, int slot_rows, size_t smem_per_cta);
+cudaError_t launch_blockdot(const GemvParams& p, bool permuted, int64_t L, int stages,
+                            int64_t ctas, cudaStream_t stream);
+cudaError_t blockdot_wait_timeouts(int reset, int* out);
 
 // Per-layout GEMV launchers (gemv_plain.cu, gemv_permuted.cu).
 cudaError_t launch_gemv_plain(const GemvParams& p, const GemvPlan& plan, cudaStream_t stream);

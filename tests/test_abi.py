@@ -145,8 +145,10 @@ BENCH_SHAPES = [(128, 256, 1), (7168, 2048, 4), (4096, 7168, 8), (7168, 16384, 1
     (BENCH_SHAPES[1], 1, -1, (1, 4, 4, 304, 64)),
     (BENCH_SHAPES[2], 1, -1, (1, 16, 1, 304, 16)),
     (BENCH_SHAPES[3], 1, -1, (1, 16, 8, 304, 32)),
-    (BENCH_SHAPES[4], 1, -1, (2, 2, 2, 608, 128)),  # >= 512 MB of A: tensor cores
+    (BENCH_SHAPES[4], 1, -1, (1, 4, 8, 304, 64)),
     (BENCH_SHAPES[4], 1, 1, (1, 4, 8, 304, 64)),
+    (BENCH_SHAPES[1], 0, 3, (3, 5, 1, 152, 128)),  # block-dot: one CTA per SM, 5 ring slots
+    (BENCH_SHAPES[3], 1, 3, (3, 11, 1, 152, 128)),
     (BENCH_SHAPES[0], 0, 0, (0, 4, 1, 64, 8)),
     (BENCH_SHAPES[1], 0, 0, (0, 32, 1, 304, 8)),
     (BENCH_SHAPES[2], 0, 0, (0, 16, 1, 304, 8)),
@@ -160,23 +162,24 @@ def test_plan_for_the_benchmark_shapes(lib, shape, layout, kernel, want):
     assert got == want
     if plan["kernel"] == nv.KERNEL_TENSOR:  # lanes_per_row = stages; steps = 256-element K stages
         assert plan["steps"] == -(-K // 256) and plan["threads_per_cta"] == 224
+    elif plan["kernel"] == nv.KERNEL_BLOCKDOT:  # lanes_per_row = ring slots; 512-element stages
+        assert plan["steps"] == -(-K // 512) and plan["threads_per_cta"] == 192
     else:
         assert plan["steps"] == -(-(K // 64) // plan["lanes_per_row"])
 
 
 def test_tensor_kernel_plans(lib):
-    """The tensor-core kernel: pre-permuted scales only; chosen by default for
-    GEMVs with at least 512 MB of A; its schedule follows the measured rule
-    (2 stages, the smallest cluster filling 70% of 4 resident CTAs per SM, at
-    least 2 for 16+ K stages, persistent clusters no more than the tiles)."""
+    """The tensor-core kernel: pre-permuted scales only, selected explicitly
+    (nvfp4_gemv never picks it: its MMA reads scale codes as unsigned); its
+    schedule follows the measured rule (2 stages, the smallest cluster filling
+    70% of 4 resident CTAs per SM, at least 2 for 16+ K stages, persistent
+    clusters no more than the tiles)."""
     with pytest.raises(nv.Nvfp4Error):
         nv.nvfp4_gemv_plan(4096, 7168, 8, 0, 152, 2, kernel=nv.KERNEL_TENSOR)
-    assert nv.nvfp4_gemv_plan(16384, 8192, 16, 0, 152, 2)["kernel"] == nv.KERNEL_PIPELINED
-    assert nv.nvfp4_gemv_plan(16384, 8192, 2, 1, 152, 2)["kernel"] == nv.KERNEL_PIPELINED
-    assert nv.nvfp4_gemv_plan(16384, 8192, 8, 1, 152, 2)["kernel"] == nv.KERNEL_TENSOR
-    # more tiles than 32-bit tile coordinates hold: the pipelined kernel
-    assert nv.nvfp4_gemv_plan(1, 1024, 1 << 31, 1, 152, 2)["kernel"] == nv.KERNEL_PIPELINED
-    assert nv.nvfp4_gemv_plan(1, 1024, (1 << 31) - 1, 1, 152, 2)["kernel"] == nv.KERNEL_TENSOR
+    for shape in ((16384, 8192, 16), (16384, 8192, 2), (16384, 8192, 8), (1, 1024, 1 << 31),
+                  (1, 1024, (1 << 31) - 1)):
+        for layout in (0, 1):
+            assert nv.nvfp4_gemv_plan(*shape, layout, 152, 2)["kernel"] == nv.KERNEL_PIPELINED
     rng = np.random.default_rng(1)
     for _ in range(200):
         M, K, L = int(rng.integers(1, 30000)), 64 * int(rng.integers(1, 400)), int(rng.integers(1, 9))
@@ -187,6 +190,31 @@ def test_tensor_kernel_plans(lib):
         assert plan["lanes_per_row"] == 2 and ks in (1, 2, 4, 8) and (ks == 1 or ks <= kst)
         assert plan["ctas"] % ks == 0 and plan["ctas"] // ks <= tiles
         assert plan["ctas"] <= max(ks, 4 * sms)
+
+
+def test_block_dot_plans_and_validation(lib):
+    """The block-dot kernel, selected explicitly: one CTA per SM (no more than
+    the 8-row units), the deepest ring that fits; plain scales need K % 256 == 0."""
+    for M, K, L, layout in ((7168, 2048, 4, 0), (7168, 16384, 1, 1), (1, 64, 1, 1), (9, 512, 3, 0),
+                            (100000, 64, 1, 1)):
+        plan = nv.nvfp4_gemv_plan(M, K, L, layout, 152, 2, kernel=nv.KERNEL_BLOCKDOT)
+        units = L * -(-M // 8)
+        cb = 2 if K % 256 == 0 else 1
+        assert plan["kernel"] == nv.KERNEL_BLOCKDOT and plan["k_split"] == 1
+        assert plan["ctas"] == min(152, units) and 2 <= plan["lanes_per_row"] <= 32
+        assert plan["steps"] == -(-(K // 64) // (4 * cb)) and plan["threads_per_cta"] == 192
+    with pytest.raises(nv.Nvfp4Error):  # plain scales, K % 256 != 0
+        nv.nvfp4_gemv_plan(128, 320, 1, 0, 152, 2, kernel=nv.KERNEL_BLOCKDOT)
+    args = (64, 64, 64, 64, 64, 300, 1024, 2, nv.SF_PLAIN)
+    B = nv.KERNEL_BLOCKDOT
+    assert lib.nvfp4_gemv_explicit(*args, B, 4, 2, 8, None) == nv.ERR_INVALID_VALUE   # k_split
+    assert lib.nvfp4_gemv_explicit(*args, B, 1, 1, 8, None) == nv.ERR_INVALID_VALUE   # 1 slot
+    assert lib.nvfp4_gemv_explicit(*args, B, 33, 1, 8, None) == nv.ERR_INVALID_VALUE  # > 32 slots
+    assert lib.nvfp4_gemv_explicit(*args, B, 4, 1, 0, None) == nv.ERR_INVALID_VALUE   # no CTA
+    plain320 = args[:6] + (320,) + args[7:]
+    assert lib.nvfp4_gemv_explicit(*plain320, B, 4, 1, 8, None) == nv.ERR_UNSUPPORTED_SHAPE
+    empty = args[:5] + (0,) + args[6:]
+    assert lib.nvfp4_gemv_explicit(*empty, B, 4, 1, 8, None) == nv.OK
 
 
 def max_rows_per_row_lane(M, L, perm, lpr, ks, ctas):
