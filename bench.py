@@ -1,23 +1,36 @@
 """Benchmark: NVFP4 block-scaled batched GEMV on GB300, through the C ABI.
 
-Default workload: M=7168, K=2048, L=4 (33.1 MB per call), the first of the
-three shapes the submissions time.  One step is one ``nvfp4_gemv`` call,
-the whole hot path.
+Headline workload: M=16384, K=8192, L=16 (1.21 GB per call, plain scales), the
+largest of the five workloads.  One step is one ``nvfp4_gemv`` call, the whole
+hot path.
 
 Timed region (``value``): K back-to-back calls replayed from a CUDA graph,
-bracketed by CUDA events on the launching stream.  Consecutive calls rotate
-over 8 resident copies of the inputs (8 x 33 MB > 2x the 129 MB L2), so every
-call reads its operands from HBM (cold L2).  ``value`` = elapsed / K in
-microseconds per call.
+bracketed by CUDA events on the launching stream; that K-call window is
+repeated R times (until the windows add up to at least 0.5 s) and ``value``
+is the median over the windows of elapsed / K, in microseconds per call.
+Consecutive calls rotate over resident copies of the inputs (at least 2, and
+together more than 2x the 129 MB L2), so every call reads its operands from
+HBM (cold L2).  Consecutive calls do overlap: each call is launched with
+programmatic stream serialization, so its CTAs start (and prefetch their first
+lines of A into L2) while the previous call's last CTAs finish.  Each line
+therefore also carries ``single_call_l2_flushed_us``: one event-bracketed call
+after writing a buffer of twice the L2 size, nothing overlapping it.
+
+Before the headline line, one line per (workload, scale layout) of the other
+workloads (the pages' three timed shapes, the small parity shape, and the
+headline shape with pre-permuted scales) gives the same two figures
+(``--no-extra`` skips them).
 
 ``e2e``: the same call through the C ABI with host buffers: each step copies
 a, b, sfa, sfb from pinned host memory, runs the GEMV and copies c back.
 
-``--impl reference``: the CPU oracle timed on the host cores on a bounded
-sample of the same workload, reported in the same unit.
+``cpu_baseline`` and ``--impl reference``: the CPU oracle on the host cores
+(every core, one thread per core over disjoint rows) on a bounded sample of
+the same workload, scaled to a whole call; the one-core figure is given beside
+it.
 
-Run ``python bench.py --all-configs`` to also time every workload and scale
-layout (extra JSON lines, after the main one).
+``--all-configs`` also times the scale repack, the extended entry point and
+the small-N GEMM (extra JSON lines after the headline).
 """
 from __future__ import annotations
 
@@ -40,8 +53,9 @@ from nvfp4_block_scaled_gemv_gb300 import synthetic  # noqa: E402
 
 METRIC = "us/call (cold L2) and achieved HBM GB/s as % of GB300 peak, NVFP4 GEMV"
 UNIT = "us/call"
-WORKLOAD = synthetic.WORKLOADS[1]  # ("M7168_K2048_L4", 7168, 2048, 4)
+WORKLOAD = synthetic.WORKLOADS[4]  # ("M16384_K8192_L16", 16384, 8192, 16)
 ROTATE_SETS = 8
+MIN_WINDOW_S = 0.5  # the timed K-call windows add up to at least this
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -51,12 +65,17 @@ REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=192000)
-    ap.add_argument("--warmup", type=int, default=6400)
+    ap.add_argument("--steps", type=int, default=20,
+                    help="calls per timed window (each window is timed on its own)")
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--layout", choices=["plain", "permuted"], default="plain")
-    ap.add_argument("--all-configs", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the per-workload lines printed before the headline")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="also time the scale repack, the extended entry point and the "
+                         "small-N GEMM (lines after the headline)")
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--workload", default=WORKLOAD[0],
                     choices=[w[0] for w in synthetic.WORKLOADS])
     ap.add_argument("--ncu", action="store_true",
@@ -64,6 +83,10 @@ def parse_args():
     ap.add_argument("--schedule", default=None,
                     help="with --ncu: KERNEL,LANES_PER_ROW,K_SPLIT,CTAS for nvfp4_gemv_explicit "
                          "instead of the chosen schedule")
+    ap.add_argument("--rotate", type=int, default=0,
+                    help="with --ncu: calls rotate over this many input sets (default 2)")
+    ap.add_argument("--graph", action="store_true",
+                    help="with --ncu: replay the --steps calls from one CUDA graph")
     ap.add_argument("--gemm-workload", default=None,
                     help="with --ncu: run nvfp4_gemm_small_n on this decode-batch workload "
                          "(e.g. M7168_N8_K2048_L4) instead of the GEMV")
@@ -137,12 +160,10 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self, t0: float, t1: float) -> dict:
+        # only samples taken inside the timed region count
         inside = [p for t, p in self.samples if t0 <= t <= t1]
         if not inside:
-            inside = [p for _, p in self.samples]
-        if not inside:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
-                    "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         sm = [float(p[1]) for p in inside if p[1].replace(".", "", 1).isdigit()]
         smax = [float(p[2]) for p in inside if p[2].replace(".", "", 1).isdigit()]
         reasons = set()
@@ -172,15 +193,15 @@ def gpu_id_for_smi(torch, dev_index: int) -> str:
 # helpers
 # ---------------------------------------------------------------------------
 
-# The files of the CUDA-core GEMV kernels' code: everything under csrc/ but the
-# separate scale-repack and tensor-core kernels and the host planner (whose
-# choice is checked through the recorded schedule instead).
-_NOT_KERNEL_CODE = ("repack.cu", "gemv_tc.cu", "api.cu")
+# The GEMV kernels' code: everything under csrc/ but the separate scale-repack
+# kernel and the host planner (whose choice is checked through the recorded
+# schedule instead).
+_NOT_KERNEL_CODE = ("repack.cu", "api.cu")
 _SCHEDULE_KEYS = ("kernel", "lanes_per_row", "k_split", "ctas")
 
 
 def kernel_source_hash() -> str:
-    """Hash of the CUDA-core GEMV kernels' sources."""
+    """Hash of the GEMV kernels' sources."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_block_scaled_gemv_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
@@ -267,8 +288,15 @@ class ExtProblem(DeviceProblem):
                          b_batch_stride=self.b_stride, stream=stream_handle)
 
 
-def time_graph(torch, nv, prob, steps, warmup, stream):
-    """Per-call microseconds over `steps` calls replayed from a CUDA graph."""
+def time_graph(torch, nv, prob, steps, warmup, stream, min_window_s=MIN_WINDOW_S):
+    """Microseconds per call over windows of `steps` back-to-back calls.
+
+    The calls are captured once into a CUDA graph (of g calls, g a divisor of
+    `steps`, replayed steps/g times per window).  Each window is bracketed by
+    its own pair of CUDA events on the launching stream; windows follow one
+    another until they add up to min_window_s.  Returns (median us per call
+    over the windows, (t0, t1) host monotonic bounds of the timed region,
+    calls timed, windows)."""
     handle = stream.cuda_stream
     g_size = max(d for d in range(1, min(64, steps) + 1) if steps % d == 0)
     with torch.cuda.stream(stream):
@@ -279,30 +307,47 @@ def time_graph(torch, nv, prob, steps, warmup, stream):
     with torch.cuda.graph(graph, stream=stream):
         for i in range(g_size):
             prob.call(nv, i, handle)
+    # warm the graph and estimate one window's length
     with torch.cuda.stream(stream):
-        for _ in range(2):
-            graph.replay()
-    stream.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    t0 = time.monotonic()
-    with torch.cuda.stream(stream):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        graph.replay()
         e0.record(stream)
         for _ in range(steps // g_size):
             graph.replay()
         e1.record(stream)
     stream.synchronize()
+    est_s = max(e0.elapsed_time(e1) * 1e-3, 1e-6)
+    windows = max(1, min(100000, int(min_window_s / est_s) + 1))
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(windows)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    with torch.cuda.stream(stream):
+        for s0, s1 in events:
+            s0.record(stream)
+            for _ in range(steps // g_size):
+                graph.replay()
+            s1.record(stream)
+    stream.synchronize()
     t1 = time.monotonic()
     torch.cuda.synchronize()
     barrier()
-    return e0.elapsed_time(e1) * 1e3 / steps, (t0, t1), steps
+    per_call = [s0.elapsed_time(s1) * 1e3 / steps for s0, s1 in events]
+    return statistics.median(per_call), (t0, t1), steps * windows, windows
+
+
+def l2_bytes(torch, dev) -> int:
+    props = torch.cuda.get_device_properties(dev)
+    return int(getattr(props, "L2_cache_size", 0) or 132 * 2 ** 20)
 
 
 def time_single_flushed(torch, nv, prob, reps, stream):
-    """Median microseconds of one event-bracketed call after an L2 flush."""
-    flush = torch.empty(2 * 160 * 2 ** 20, dtype=torch.uint8, device=prob.sets[0]["a"].device)
+    """Median and min microseconds of one event-bracketed call, each after
+    writing a buffer of twice the L2 size (nothing else runs in the bracket)."""
+    dev = prob.sets[0]["a"].device
+    flush = torch.empty(2 * l2_bytes(torch, dev), dtype=torch.uint8, device=dev)
     handle = stream.cuda_stream
     times = []
     with torch.cuda.stream(stream):
@@ -335,7 +380,7 @@ def time_e2e(torch, nv, p, M, K, L, dev, steps, stream):
         c_host.copy_(c, non_blocking=True)
 
     with torch.cuda.stream(stream):
-        for _ in range(5):
+        for _ in range(3):
             step()
         stream.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -347,6 +392,7 @@ def time_e2e(torch, nv, p, M, K, L, dev, steps, stream):
     stream.synchronize()
     h2d = sum(v.numel() * v.element_size() for k, v in host.items())
     d2h = c_host.numel() * c_host.element_size()
+    del host, d, c, c_host
     return e0.elapsed_time(e1) * 1e3 / steps, h2d, d2h
 
 
@@ -354,28 +400,45 @@ def time_e2e(torch, nv, p, M, K, L, dev, steps, stream):
 # CPU oracle baseline
 # ---------------------------------------------------------------------------
 
-def oracle_us_per_call(p, M, K, L, budget_s: float):
-    """The oracle on one host core over a bounded sample of rows, scaled to a
-    full call.  Returns (us_per_call, sample description)."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def oracle_us_per_call(p, M, K, L, budget_s: float, threads: int = 1):
+    """The oracle on `threads` host cores over a bounded sample of outputs,
+    scaled to a full call.  Each thread evaluates its own random outputs (the
+    oracle's C routine runs without the interpreter lock); the oracle itself
+    is unchanged.  Returns (us_per_call, sample description)."""
+    import concurrent.futures
+
     import oracle
 
+    oracle.build()
     rows = L * M
-    n = 256
     rng = np.random.default_rng(0)
+    n = 64
     spent, done = 0.0, 0
-    while True:
-        li = rng.integers(0, L, n)
-        mi = rng.integers(0, M, n)
-        t0 = time.perf_counter()
+
+    def work(idx):
+        li, mi = idx
         oracle.gemv_at(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L, mi, li)
-        spent += time.perf_counter() - t0
-        done += n
-        if spent >= budget_s:
-            break
-        n = min(8192, n * 2)
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as pool:
+        while True:
+            chunks = [(rng.integers(0, L, n), rng.integers(0, M, n)) for _ in range(threads)]
+            t0 = time.perf_counter()
+            list(pool.map(work, chunks))
+            spent += time.perf_counter() - t0
+            done += n * threads
+            if spent >= budget_s:
+                break
+            n = min(8192, n * 2)
     us = spent / done * rows * 1e6
     return us, (f"{done} random outputs (full K each) of the {rows}-output call in {spent:.2f} s "
-                "on one core, scaled to the whole call")
+                f"of wall time on {threads} host core(s), scaled to the whole call")
 
 
 # ---------------------------------------------------------------------------
@@ -386,15 +449,16 @@ def run_reference(args):
     rank, world, _ = rank_info()
     if rank != 0:
         return
-    name, M, K, L = WORKLOAD
+    name, M, K, L = next(w for w in synthetic.WORKLOADS if w[0] == args.workload)
     p = synthetic.make_problem(M, K, L, seed=0)
+    cores = host_cores()
     # every step is one bounded sample; the whole run stays within about a minute
     per_step_budget = max(0.02, min(10.0, 60.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        oracle_us_per_call(p, M, K, L, per_step_budget / 4)
+        oracle_us_per_call(p, M, K, L, per_step_budget / 4, cores)
     vals, samples = [], []
     for _ in range(args.steps):
-        us, sample = oracle_us_per_call(p, M, K, L, per_step_budget)
+        us, sample = oracle_us_per_call(p, M, K, L, per_step_budget, cores)
         vals.append(us)
         samples.append(sample)
     value = statistics.median(vals)
@@ -404,12 +468,48 @@ def run_reference(args):
         "ms_per_step": round(value / 1e3, 6), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": name, "M": M, "K": K, "L": L, "scale_layout": "plain"},
-        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": samples[-1]},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def rotating_sets(nbytes: int) -> int:
+    """Input copies to rotate over: together more than 400 MB (> 2x L2), at least 2."""
+    return max(2, min(ROTATE_SETS, -(-400 * 2 ** 20 // nbytes)))
+
+
+def kernel_name(nv, torch, dev, M, K, L, layout) -> str:
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    plan = nv.nvfp4_gemv_plan(M, K, L, layout, sms)
+    return ["direct", "pipelined", "tensor"][plan["kernel"]]
+
+
+def config_line(torch, nv, dev, stream, peaks, wname, wM, wK, wL, lay_name, steps, warmup):
+    """One (workload, layout): graph-replayed back-to-back calls and single
+    L2-flushed calls, as a compact JSON line."""
+    lay = nv.SF_PLAIN if lay_name == "plain" else nv.SF_PERMUTED_128x4
+    wp = synthetic.make_problem(wM, wK, wL, seed=0)
+    wbytes = synthetic.algorithmic_bytes(wM, wK, wL)
+    sets = rotating_sets(wbytes)
+    wprob = DeviceProblem(torch, nv, wp, wM, wK, wL, lay, dev, sets)
+    wsteps = max(steps, 64)
+    wus, _, calls, windows = time_graph(torch, nv, wprob, wsteps, max(warmup, 16), stream,
+                                        min_window_s=0.25)
+    smed, smin = time_single_flushed(torch, nv, wprob, 20, stream)
+    gbs = wbytes / (wus * 1e-6) / 1e9
+    sgbs = wbytes / (smed * 1e-6) / 1e9
+    del wprob
+    torch.cuda.empty_cache()
+    return {"kind": "per_workload", "workload": wname, "scale_layout": lay_name,
+            "kernel": kernel_name(nv, torch, dev, wM, wK, wL, lay),
+            "bytes_per_call": wbytes, "us_per_call": round(wus, 3), "gb_per_s": round(gbs, 1),
+            "pct_of_hbm_peak": round(100 * gbs / peaks["hbm_gbs"], 2),
+            "single_call_l2_flushed_us": round(smed, 3),
+            "single_call_pct_of_hbm_peak": round(100 * sgbs / peaks["hbm_gbs"], 2),
+            "rotating_sets": sets, "calls": calls, "windows": windows}
 
 
 def run_native(args):
@@ -428,31 +528,51 @@ def run_native(args):
     libbuild.build()
     nv.library()
     stream = torch.cuda.Stream(device=dev)
+    peaks = measured_peaks()
 
     name, M, K, L = next(w for w in synthetic.WORKLOADS if w[0] == args.workload)
     layout = nv.SF_PLAIN if args.layout == "plain" else nv.SF_PERMUTED_128x4
+
+    # the other workloads and layouts first (the headline line is printed last)
+    per_workload = []
+    if not args.no_extra:
+        for wname, wM, wK, wL in synthetic.WORKLOADS:
+            for lay_name in ("plain", "permuted"):
+                if (wname, lay_name) == (name, args.layout):
+                    continue
+                line = config_line(torch, nv, dev, stream, peaks, wname, wM, wK, wL, lay_name,
+                                   args.steps, args.warmup)
+                per_workload.append(line)
+                if rank == 0:
+                    print(json.dumps(line), flush=True)
+
     p = synthetic.make_problem(M, K, L, seed=0)
     nbytes = synthetic.algorithmic_bytes(M, K, L)
-    sets = max(2, min(ROTATE_SETS, -(-400 * 2 ** 20 // nbytes)))
+    sets = rotating_sets(nbytes)
     prob = DeviceProblem(torch, nv, p, M, K, L, layout, dev, sets)
 
     sampler = ClockSampler(gpu_id_for_smi(torch, local)) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
-    us, (t0, t1), steps = time_graph(torch, nv, prob, args.steps, args.warmup, stream)
+    us, (t0, t1), calls, windows = time_graph(torch, nv, prob, args.steps, args.warmup, stream)
     if sampler:
         sampler.stop()
-    us_job = max_over_ranks(us * steps) / (steps * world)  # all ranks' calls / slowest rank
+    us_job = max_over_ranks(us) / world  # all ranks' calls / the slowest rank's time
     us_rank = max_over_ranks(us)
 
-    single_med, single_min = time_single_flushed(torch, nv, prob, 50, stream)
-    e2e_us, h2d, d2h = time_e2e(torch, nv, p, M, K, L, dev, args.e2e_steps, stream)
-    e2e_us = max_over_ranks(e2e_us)
+    single_med, single_min = time_single_flushed(torch, nv, prob, 30, stream)
+    del prob
+    torch.cuda.empty_cache()
+    e2e_steps = max(5, min(args.e2e_steps, int(4e9 / nbytes)))
+    e2e_us, h2d, d2h = time_e2e(torch, nv, p, M, K, L, dev, e2e_steps, stream)
+    e2e_us = max_over_ranks(e2e_us) / world
 
     if rank != 0:
         return
-    cpu_us, cpu_sample = oracle_us_per_call(p, M, K, L, budget_s=10.0)
-    peaks = measured_peaks()
+    cores = host_cores()
+    cpu_us, cpu_sample = oracle_us_per_call(p, M, K, L, budget_s=10.0, threads=cores)
+    cpu1_us, _ = oracle_us_per_call(p, M, K, L, budget_s=3.0, threads=1)
     achieved = nbytes / (us_rank * 1e-6) / 1e9
+    single_gbs = nbytes / (single_med * 1e-6) / 1e9
     plan = nv.nvfp4_gemv_plan(M, K, L, layout, torch.cuda.get_device_properties(dev).multi_processor_count)
     line = {
         "metric": METRIC, "value": round(us_job, 4), "unit": UNIT, "n_gpus": world,
@@ -462,45 +582,33 @@ def run_native(args):
         "config": {"workload": name, "M": M, "K": K, "L": L, "scale_layout": args.layout,
                    "l2": f"{sets} rotating input sets, {sets * nbytes / 1e6:.0f} MB "
                          "> 2x L2 (cold L2 every call)",
-                   "launch": "CUDA graph of back-to-back nvfp4_gemv calls, PDL",
-                   "bytes_per_call": nbytes, "schedule": plan},
+                   "launch": "CUDA graph of back-to-back nvfp4_gemv calls with programmatic "
+                             "stream serialization: each call's CTAs start, and prefetch their "
+                             "first A lines into L2, while the previous call's last CTAs finish",
+                   "timing": f"{windows} event-bracketed windows of {args.steps} calls, median",
+                   "bytes_per_call": nbytes, "schedule": plan,
+                   "kernel": ["direct", "pipelined", "tensor"][plan["kernel"]]},
         "gb_per_s": round(achieved, 1),
         "pct_of_hbm_peak": round(100 * achieved / peaks["hbm_gbs"], 2),
-        "single_call_l2_flushed_us": {"median": round(single_med, 3), "min": round(single_min, 3)},
+        "single_call_l2_flushed_us": {"median": round(single_med, 3), "min": round(single_min, 3),
+                                      "pct_of_hbm_peak": round(100 * single_gbs / peaks["hbm_gbs"], 2)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": profiled_traffic(name, args.layout, plan),
                      "peak_source": peaks["source"]},
-        "cpu_baseline": {"value": round(cpu_us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": cpu_sample},
+        "cpu_baseline": {"value": round(cpu_us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": cpu_sample, "one_core_value": round(cpu1_us, 1)},
         "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": steps,
+        "gpu_launches": calls,
         "clocks": sampler.summary(t0, t1) if sampler else None,
+        "per_workload": [{k: w[k] for k in ("workload", "scale_layout", "kernel", "us_per_call",
+                                             "pct_of_hbm_peak", "single_call_l2_flushed_us")}
+                         for w in per_workload],
     }
     print(json.dumps(line), flush=True)
 
     if args.all_configs:
-        for wname, wM, wK, wL in synthetic.WORKLOADS:
-            wp = synthetic.make_problem(wM, wK, wL, seed=0)
-            wbytes = synthetic.algorithmic_bytes(wM, wK, wL)
-            sets = max(2, min(ROTATE_SETS, -(-400 * 2 ** 20 // wbytes)))
-            for lay_name, lay in (("plain", nv.SF_PLAIN), ("permuted", nv.SF_PERMUTED_128x4)):
-                wprob = DeviceProblem(torch, nv, wp, wM, wK, wL, lay, dev, sets)
-                wsteps = max(64, min(20000, int(2e9 / wbytes)) // 64 * 64)
-                wus, _, _ = time_graph(torch, nv, wprob, wsteps, 64, stream)
-                smed, smin = time_single_flushed(torch, nv, wprob, 20, stream)
-                gbs = wbytes / (wus * 1e-6) / 1e9
-                kname = ["direct", "pipelined", "tensor"][
-                    nv.nvfp4_gemv_plan(wM, wK, wL, lay, num_sms=torch.cuda.get_device_properties(
-                        dev).multi_processor_count)["kernel"]]
-                print(json.dumps({"workload": wname, "scale_layout": lay_name, "kernel": kname,
-                                  "us_per_call": round(wus, 3), "gb_per_s": round(gbs, 1),
-                                  "pct_of_hbm_peak": round(100 * gbs / peaks["hbm_gbs"], 2),
-                                  "rotating_sets": sets, "calls": wsteps,
-                                  "single_call_l2_flushed_us": round(smed, 3)}), flush=True)
-                del wprob
-                torch.cuda.empty_cache()
         # the scale repack (plain -> 128x4 atoms) of each workload's sfa, graph-replayed
         # over rotating buffers; bytes = plain scales read + permuted atoms written
         for wname, wM, wK, wL in synthetic.WORKLOADS:
@@ -518,8 +626,8 @@ def run_native(args):
                     nv_.nvfp4_repack_scales(srcs[i % sets].data_ptr(), dsts[i % sets].data_ptr(),
                                             wM, wK, wL, h)
 
-            rsteps = max(64, min(20000, int(2e9 / rbytes)) // 64 * 64)
-            rus, _, _ = time_graph(torch, nv, _Repack(), rsteps, 64, stream)
+            rsteps = 64
+            rus, _, _, _ = time_graph(torch, nv, _Repack(), rsteps, 64, stream, 0.25)
             gbs = rbytes / (rus * 1e-6) / 1e9
             print(json.dumps({"workload": wname, "kernel": "repack_scales (sfa)",
                               "us_per_call": round(rus, 3), "bytes_per_call": rbytes,
@@ -529,12 +637,12 @@ def run_native(args):
             del srcs, dsts
             torch.cuda.empty_cache()
         # the extended entry point on the headline shape
-        wname, wM, wK, wL = WORKLOAD
+        wname, wM, wK, wL = synthetic.WORKLOADS[1]
         wp = synthetic.make_problem(wM, wK, wL, seed=0)
         wbytes = synthetic.algorithmic_bytes(wM, wK, wL) + 2 * wL * wM  # + the bias
         wprob = ExtProblem(torch, nv, wp, wM, wK, wL, nv.SF_PLAIN, dev, ROTATE_SETS)
-        wsteps = max(64, min(20000, int(2e9 / wbytes)) // 64 * 64)
-        wus, _, _ = time_graph(torch, nv, wprob, wsteps, 64, stream)
+        wsteps = 64
+        wus, _, _, _ = time_graph(torch, nv, wprob, wsteps, 64, stream, 0.25)
         gbs = wbytes / (wus * 1e-6) / 1e9
         print(json.dumps({"workload": wname, "scale_layout": "plain",
                           "path": "nvfp4_gemv_ex: alpha 0.5, fp16 bias, b in an [L][8][K/2] buffer",
@@ -564,8 +672,8 @@ def run_native(args):
                                            x[3].data_ptr(), x[4].data_ptr(), gM, gN, gK, gL,
                                            stream=h)
 
-            gsteps = max(64, min(20000, int(2e9 / gbytes)) // 64 * 64)
-            gus, _, _ = time_graph(torch, nv, _Gemm(), gsteps, 64, stream)
+            gsteps = 64
+            gus, _, _, _ = time_graph(torch, nv, _Gemm(), gsteps, 64, stream, 0.25)
             gbs = gbytes / (gus * 1e-6) / 1e9
             print(json.dumps({"workload": gname, "path": "nvfp4_gemm_small_n (tensor cores)",
                               "N": gN, "us_per_call": round(gus, 3), "bytes_per_call": gbytes,
@@ -617,10 +725,11 @@ def run_profile_case(args):
         stream.synchronize()
         print(f"profile case done: {name} sfa repack {args.warmup}+{args.steps} calls")
         return
-    prob = DeviceProblem(torch, nv, p, M, K, L, layout, dev, 2)
+    prob = DeviceProblem(torch, nv, p, M, K, L, layout, dev, args.rotate or 2)
     torch.cuda.synchronize()
     sched = [int(v) for v in args.schedule.split(",")] if args.schedule else None
-    for i in range(args.warmup + args.steps):
+
+    def one(i):
         if sched is None:
             prob.call(nv, i, stream.cuda_stream)
         else:
@@ -628,8 +737,24 @@ def run_profile_case(args):
             nv.nvfp4_gemv_explicit(s["a"].data_ptr(), s["b"].data_ptr(), s["sfa"].data_ptr(),
                                    s["sfb"].data_ptr(), s["c"].data_ptr(), M, K, L, layout,
                                    *sched, stream=stream.cuda_stream)
+
+    if args.graph:
+        # the benchmark's launch form: the calls replayed from one CUDA graph
+        # (warm-up calls run eagerly before the capture)
+        for i in range(args.warmup):
+            one(i)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(args.steps):
+                one(i)
+        graph.replay()
+    else:
+        for i in range(args.warmup + args.steps):
+            one(i)
     stream.synchronize()
-    print(f"profile case done: {name} {args.layout} {args.warmup}+{args.steps} calls")
+    print(f"profile case done: {name} {args.layout} {args.warmup}+{args.steps} calls "
+          f"over {len(prob.sets)} input sets{' (graph)' if args.graph else ''}")
 
 
 def main():

@@ -60,6 +60,13 @@ def test_max_over_ranks_is_identity_without_a_process_group():
     bench.barrier()  # a no-op outside torch.distributed
 
 
+def bench_host_cores():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    return bench.host_cores()
+
+
 def _run_reference(env_extra):
     env = {**os.environ, **env_extra}
     return subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
@@ -83,4 +90,5 @@ def test_reference_arm_line_on_rank_zero():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
                            "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
-    assert line["config"]["workload"] == "M7168_K2048_L4"
+    assert line["config"]["workload"] == "M16384_K8192_L16"
+    assert line["cpu_baseline"]["cores"] == bench_host_cores()
