@@ -82,8 +82,8 @@ typedef enum {
  * NULL).  Limits: K <= 2^30, M*L < 2^40.
  * Alignment: a, b, sfa, sfb 32-byte aligned; c 2-byte aligned.
  * Accuracy: on the CUDA-core kernels each 16-element block's dot product is
- * exact and blocks are scaled and summed in FP32; the tensor-core kernel
- * (pre-permuted scales with at least 512 MB of A) sums in the MMA's FP32 order.
+ * exact and blocks are scaled and summed in FP32 (nvfp4_gemv always runs one
+ * of them).
  * c is rounded to nearest even (overflow gives +-Inf; a NaN scale gives NaN)
  * and stays within 1e-3 * sum|terms| + 1 fp16 ulp of the exact result.
  * Results are bitwise reproducible run to run.  The FP32 summation order
@@ -154,10 +154,25 @@ typedef enum {
    * persistent over the L*ceil(M/128) tiles); lanes_per_row = pipeline
    * stages per CTA (2 or 4: 4, 3 or 2 CTAs of 2 stages share an SM, 2 of 4).
    * The MMA sums in fp32 in an order of its own: c meets the same accuracy
-   * contract, not the CUDA-core kernels' bits.  nvfp4_gemv picks it for
-   * pre-permuted scales with at least 512 MB of A (where it streams faster);
-   * the pipelined kernel otherwise. */
-  NVFP4_KERNEL_TENSOR = 2
+   * contract, not the CUDA-core kernels' bits.  The MMA reads scale codes as
+   * unsigned magnitudes; the kernel folds every negative sfa or sfb code into
+   * the sign bits of the 16 elements it scales before the MMA, so signed,
+   * subnormal and NaN codes give the E4M3 result.  Selected explicitly only
+   * (nvfp4_gemv picks the CUDA-core kernels; nvfp4_gemm_small_n uses it for
+   * N >= 2). */
+  NVFP4_KERNEL_TENSOR = 2,
+  /* Tensor-core block dots with the scales applied on the CUDA cores: A is
+   * streamed by TMA in one box per tile of up to 128 rows (rows handed out to
+   * one CTA per SM in units of 8), 512-element K stages (256 when K % 256 !=
+   * 0), a ring of lanes_per_row slots (2..32; 0 = the most that fit); the
+   * block-scaled MMA runs with unit A scales and constant selector B scales
+   * so that it writes each 16-element block's dot to its own accumulator
+   * column, and the epilogue adds dot * sfa * sfb in fp32 from the signed
+   * E4M3 codes, block by block in K order (bits independent of grid, ring
+   * depth and scale layout).  k_split must be 1.  Plain scales need
+   * K % 256 == 0.  Selected explicitly only: measured on GB300 it matches the
+   * pipelined kernel on the largest streams and is slower on smaller ones. */
+  NVFP4_KERNEL_BLOCKDOT = 3
 } nvfp4_kernel_t;
 
 /*
@@ -259,23 +274,27 @@ int nvfp4_tensor_wait_timeouts(int reset);
  * nvfp4_kernel_t value that kernel's plan (NVFP4_ERR_UNSUPPORTED_SHAPE if it
  * cannot run the shape).  num_sms is the device's multiprocessor count and
  * ctas_per_sm the number of the CUDA-core kernel's CTAs resident per SM (pass
- * 0 to use the compiled-in default of 2).  nvfp4_gemv picks: the tensor-core
- * kernel for pre-permuted scales with at least 512 MB of A; the direct kernel
- * for K = 0 and for plain scales up to 512 KB of A; the pipelined kernel
- * otherwise.  For the tensor-core kernel the plan assumes 4 resident CTAs per
- * SM; a launch recomputes its grid from the device's limits.
+ * 0 to use the compiled-in default of 2).  nvfp4_gemv picks: the direct
+ * kernel for K = 0 and for plain scales up to 512 KB of A; the pipelined
+ * kernel otherwise.  For the tensor-core kernel the plan assumes 4 resident
+ * CTAs per SM (a launch recomputes its grid from the device's limits); for
+ * the block-dot kernel, one CTA per SM and up to 227 KB of shared memory.
  */
 typedef struct {
   int kernel;         /* nvfp4_kernel_t */
   int lanes_per_row;  /* lanes of a warp that share one row (32-byte K chunk
-                         each); tensor-core kernel: pipeline stages per CTA */
+                         each); tensor-core kernel: pipeline stages per CTA;
+                         block-dot kernel: ring slots */
   int k_split;        /* warps of a CTA that split one row's K range;
-                         tensor-core kernel: CTAs per cluster */
-  int rows_per_pass;  /* rows a warp reduces at once; tensor-core kernel: 128 */
+                         tensor-core kernel: CTAs per cluster; block-dot: 1 */
+  int rows_per_pass;  /* rows a warp reduces at once; tensor-core and
+                         block-dot kernels: 128 (a tile) */
   int threads_per_cta;
   int64_t ctas;       /* grid size */
   int64_t steps;      /* K chunks per lane per row, ceil(K/64 / lanes_per_row);
-                         tensor-core kernel: 256-element K stages, ceil(K/256) */
+                         tensor-core kernel: 256-element K stages, ceil(K/256);
+                         block-dot kernel: ceil(K/512) (ceil(K/256) when
+                         K % 256 != 0) */
 } nvfp4_gemv_plan_t;
 
 nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, int kernel,

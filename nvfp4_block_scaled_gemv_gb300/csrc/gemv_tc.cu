@@ -38,6 +38,11 @@
 // timing or on the grid.
 // Clusters are persistent: cluster i takes tiles i, i + clusters, ...
 //
+// Scale signs: the MMA reads each scale byte as an unsigned magnitude, so
+// before a stage's MMAs the MMA warp folds every negative sfa or sfb code into
+// the sign bits of the 16 E2M1 elements it scales (fold_scale_signs); codes
+// with the sign bit clear, the benchmark's, only cost that warp a scan.
+//
 // Every wait on an mbarrier gives up after kWaitNs of global time, counts a
 // timeout in a device word the host can read, and the thread then skips its
 // remaining work; control flow stays uniform so every thread reaches the
@@ -100,6 +105,48 @@ __device__ __forceinline__ uint16_t finish_output_tc(float alpha, const uint16_t
                                                      int64_t idx) {
   const float o = bias ? fmaf(v, alpha, __half2float(__ushort_as_half(bias[idx]))) : v * alpha;
   return __half_as_ushort(__float2half_rn(o));
+}
+
+// The MMA reads each scale byte as an unsigned E4M3 magnitude (the sign bit
+// is ignored).  A negative scale is folded into the operand it scales: for
+// every scale byte of the stage with the sign bit set, the 16 E2M1 elements it
+// scales (8 bytes of one row of the A tile, or of one vector's row of the B
+// tile) get their sign bits flipped in shared memory, so the MMA's product
+// |scale| * (-x) is the signed one (exact: E2M1 negation only flips a bit).
+// A NaN code (0x7F, 0xFF) stays NaN either way.  The warp scans the stage's
+// nk sfa and nk sfb atoms, 16 bytes per lane and step; returns whether any
+// element was flipped (the caller then fences the writes for the tensor
+// cores).  B rows past the tile's 16 are never written (their atom rows are
+// padding).
+__device__ __forceinline__ bool fold_scale_signs(uint8_t* gen, uint32_t a_tile, uint32_t b_tile,
+                                                 uint32_t sfa_atoms, uint32_t sfb_atoms, int nk,
+                                                 int lane) {
+  bool flipped = false;
+  for (int j = lane; j < 2 * 32 * nk; j += 32) {
+    const bool is_b = j >= 32 * nk;
+    const int jj = is_b ? j - 32 * nk : j;  // 16-byte run: atom kk = jj / 32, atom row i = jj % 32
+    const uint4 v = *reinterpret_cast<const uint4*>(gen + (is_b ? sfb_atoms : sfa_atoms) + 16u * jj);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (((w[0] | w[1] | w[2] | w[3]) & 0x80808080u) == 0) continue;
+    const int kk = jj / 32, i = jj % 32;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+#pragma unroll
+      for (int blk = 0; blk < 4; ++blk) {
+        if (!((w[g] >> (8 * blk + 7)) & 1u)) continue;
+        const int r = 32 * g + i;  // tile row (A) or vector (B) of this scale byte
+        if (is_b && r >= 16) continue;
+        // byte 32*kk + 8*blk of row r in the 128-byte swizzled tile
+        const uint32_t unit = (uint32_t)(2 * kk + blk / 2) ^ (uint32_t)(r & 7);
+        const uint32_t off = (uint32_t)(r >> 3) * 1024u + (uint32_t)(r & 7) * 128u + unit * 16u +
+                             8u * (uint32_t)(blk & 1);
+        uint64_t* q = reinterpret_cast<uint64_t*>(gen + (is_b ? b_tile : a_tile) + off);
+        *q ^= 0x8888888888888888ull;
+        flipped = true;
+      }
+    }
+  }
+  return flipped;
 }
 
 // S: pipeline stages per CTA (2 or 4; fewer stages let more CTAs share an SM,
@@ -255,7 +302,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int s = s0 + i;
         const int nk = min(4, p.rest_k - 4 * s);
         const int st = c * SC + pos;
-        if (lane == 0 && tc::mbar_wait<false>(full_bar(st), ph, ok, &g_tc_timeouts)) {
+        if (lane == 0) tc::mbar_wait<false>(full_bar(st), ph, ok, &g_tc_timeouts);
+        __syncwarp();  // (orders lane 0's acquire before the other lanes' reads)
+        if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0) {
+          // signed scales: fold negative codes into the operands' sign bits
+          const bool flipped =
+              fold_scale_signs(gen, a_s + st * kTcABytes, b_s + st * kTcBBytes,
+                               sfa_s + st * kTcSfBytes, sfb_s + st * kTcSfBytes, nk, lane);
+          if (__any_sync(0xffffffffu, flipped))
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for the tensor cores
+          __syncwarp();
+        }
+        if (lane == 0 && ok) {
           tc::fence_after();
           for (int kk = 0; kk < nk; ++kk) {
             tc::copy_atom(tmem + kSfaCol + (uint32_t)(16 * st + 4 * kk),

@@ -54,26 +54,30 @@ def random_bytes(stream_seed: int, n: int) -> np.ndarray:
     return words.astype("<u8", copy=False).view(np.uint8)[:n].copy()
 
 
-def scale_bytes(stream_seed: int, n: int) -> np.ndarray:
-    """n E4M3 codes uniform over 0x18..0x30 (values in [1/16, 1/2])."""
+def scale_bytes(stream_seed: int, n: int, code_lo: int = SCALE_CODE_LO,
+                code_count: int = SCALE_CODE_COUNT) -> np.ndarray:
+    """n E4M3 codes uniform over code_lo .. code_lo + code_count - 1 (by
+    default 0x18..0x30, values in [1/16, 1/2])."""
     out = np.empty(n, dtype=np.uint8)
     for lo in range(0, n, _CHUNK):
         hi = min(n, lo + _CHUNK)
         w = splitmix64(stream_seed, hi - lo, start=lo)
-        out[lo:hi] = (w % np.uint64(SCALE_CODE_COUNT)).astype(np.uint8) + np.uint8(SCALE_CODE_LO)
+        out[lo:hi] = (w % np.uint64(code_count)).astype(np.uint8) + np.uint8(code_lo)
     return out
 
 
-def make_problem(M: int, K: int, L: int, seed: int = 0) -> dict:
-    """Plain-layout inputs of one batched GEMV problem, as numpy arrays."""
-    if K % 64 != 0:
-        raise ValueError("K must be a multiple of 64")
+def make_problem(M: int, K: int, L: int, seed: int = 0,
+                 scale_codes: tuple = (SCALE_CODE_LO, SCALE_CODE_COUNT)) -> dict:
+    """Plain-layout inputs of one batched GEMV problem, as numpy arrays.
+    scale_codes = (first code, number of codes) of the uniform scale draw."""
+    if K % 16 != 0:
+        raise ValueError("K must be a multiple of 16")
     base = seed * 16
     return {
         "a": random_bytes(base + STREAM_A, L * M * (K // 2)).reshape(L, M, K // 2),
         "b": random_bytes(base + STREAM_B, L * (K // 2)).reshape(L, K // 2),
-        "sfa": scale_bytes(base + STREAM_SFA, L * M * (K // 16)).reshape(L, M, K // 16),
-        "sfb": scale_bytes(base + STREAM_SFB, L * (K // 16)).reshape(L, K // 16),
+        "sfa": scale_bytes(base + STREAM_SFA, L * M * (K // 16), *scale_codes).reshape(L, M, K // 16),
+        "sfb": scale_bytes(base + STREAM_SFB, L * (K // 16), *scale_codes).reshape(L, K // 16),
     }
 
 

@@ -155,3 +155,34 @@ def test_gemm_is_deterministic():
 def test_gemm_full_size(name):
     _, M, N, K, L = next(w for w in synthetic.GEMM_WORKLOADS if w[0] == name)
     check(M, N, K, L, seed=0)
+
+
+FINITE_E4M3 = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+
+
+@pytest.mark.parametrize("M,N,K,L,schedule", [(300, 2, 1024, 3, None), (257, 16, 2304, 2, None),
+                                              (129, 5, 4096, 1, (4, 4, 8))])
+def test_gemm_every_e4m3_scale_code(M, N, K, L, schedule):
+    """sfa and every vector's sfb from all 254 finite E4M3 codes (negative,
+    -0, subnormal, 448), plus NaN codes on one row and one vector: negative
+    codes are folded into the operands' sign bits before the MMA."""
+    rng = np.random.default_rng(M * N)
+    p = {"a": rng.integers(0, 256, (L, M, K // 2), dtype=np.uint8),
+         "b": rng.integers(0, 256, (L, N, K // 2), dtype=np.uint8),
+         "sfa": rng.choice(FINITE_E4M3, (L, M, K // 16)),
+         "sfb": rng.choice(FINITE_E4M3, (L, N, K // 16))}
+    p["sfa"][0, 9, 3] = 0x7F       # one row NaN for every vector
+    p["sfb"][L - 1, 1, 20] = 0xFF  # one vector NaN for every row
+    ref, vals, tol = oracle.gemm_small_n(p["a"], p["b"], p["sfa"], p["sfb"], M, N, K, L)
+    got = run_gemm(p, M, N, K, L, schedule)
+    parity.assert_parity(got, ref, vals, tol, f"gemm all E4M3 codes M={M} N={N} K={K} L={L}")
+    v = parity.half_values(got)
+    assert np.isnan(v[0, :, 9]).all() and np.isnan(v[L - 1, 1, :]).all()
+    # a negative scale on one vector only: that vector's outputs change sign
+    q = dict(p, sfb=p["sfb"].copy())
+    q["sfb"][:, 0, :] ^= 0x80
+    flipped = parity.half_values(run_gemm(q, M, N, K, L, schedule))
+    assert np.array_equal(flipped[:, 1:, :], v[:, 1:, :], equal_nan=True)
+    base, neg = v[:, 0, :], flipped[:, 0, :]
+    fin = np.isfinite(base)
+    assert np.array_equal(np.isnan(neg), np.isnan(base)) and np.array_equal(neg[fin], -base[fin])

@@ -120,3 +120,53 @@ def test_tensor_kernel_full_size(name, ks, ctas, stages):
     _, M, K, L = next(w for w in synthetic.WORKLOADS if w[0] == name)
     p = synthetic.make_problem(M, K, L, seed=0)
     check(p, M, K, L, ks, ctas, stages)
+
+
+FINITE_E4M3 = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+
+
+@pytest.mark.parametrize("M,K,L,ks,ctas,stages", [(300, 1024, 3, 1, 3, 2), (200, 2304, 2, 2, 4, 4),
+                                                  (129, 4096, 1, 4, 8, 2)])
+def test_every_e4m3_scale_code(M, K, L, ks, ctas, stages):
+    """sfa and sfb from all 254 finite E4M3 codes (negative, -0, subnormal,
+    448) and NaN codes: the MMA reads codes as unsigned magnitudes, and the
+    kernel folds negative codes into the operands' sign bits."""
+    rng = np.random.default_rng(M + K)
+    p = {"a": rng.integers(0, 256, (L, M, K // 2), dtype=np.uint8),
+         "b": rng.integers(0, 256, (L, K // 2), dtype=np.uint8),
+         "sfa": rng.choice(FINITE_E4M3, (L, M, K // 16)),
+         "sfb": rng.choice(FINITE_E4M3, (L, K // 16))}
+    p["sfa"][0, 5, 7] = 0x7F
+    p["sfa"][L - 1, 77, 60] = 0xFF
+    if L > 1:
+        p["sfb"][0, 33] = 0xFF  # every output of batch 0 NaN
+    got = check(p, M, K, L, ks, ctas, stages)
+    v = parity.half_values(got)
+    assert np.isnan(v[0, 5]) and np.isnan(v[L - 1, 77]) and (L == 1 or np.isnan(v[0]).all())
+    assert np.signbit(v[np.isfinite(v)]).any()
+
+
+def test_each_scale_code_alone():
+    """Row m: a = b = 1.0, sfb = 1.0, sfa code m on block 0 and 0 elsewhere:
+    c[m] = 16 * E4M3(m) exactly; then every sfb code across batches."""
+    K = 256
+    table = oracle.e4m3_table()
+    want = 16.0 * table
+    nan = np.isnan(want)
+    M, L = 256, 1
+    a = np.full((L, M, K // 2), 0x22, np.uint8)
+    b = np.full((L, K // 2), 0x22, np.uint8)
+    sfa = np.zeros((L, M, K // 16), np.uint8)
+    sfa[0, :, 0] = np.arange(256, dtype=np.uint8)
+    sfb = np.full((L, K // 16), 0x38, np.uint8)
+    got = parity.half_values(run_tc(a, b, sfa, sfb, M, K, L, 1, 2, 2))[0]
+    assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], want[~nan])
+    M, L = 8, 256
+    a = np.full((L, M, K // 2), 0x22, np.uint8)
+    b = np.full((L, K // 2), 0x22, np.uint8)
+    sfa = np.zeros((L, M, K // 16), np.uint8)
+    sfa[:, :, 0] = 0x38
+    sfb = np.zeros((L, K // 16), np.uint8)
+    sfb[:, 0] = np.arange(256, dtype=np.uint8)
+    got = parity.half_values(run_tc(a, b, sfa, sfb, M, K, L, 1, 64, 4))[:, 3]
+    assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], want[~nan])
