@@ -222,8 +222,8 @@ def permuted_scale_bytes(rows: int, K: int, L: int) -> int:
 
 def repack_scales(src, rows: int, K: int, L: int) -> np.ndarray:
     """Plain scales [L, rows, K//16] -> flat 128x4-atom permuted bytes."""
-    if K % 64 != 0:
-        raise ValueError("the 128x4 atom needs K % 64 == 0")
+    if K % 16 != 0:
+        raise ValueError("scales come in 16-element blocks: K % 16 == 0")
     s = _u8(src, (L, rows, K // 16))
     out = np.zeros(permuted_scale_bytes(rows, K, L), dtype=np.uint8)
     _load().oracle_repack_scales(_p(s), _p(out), rows, K, L)

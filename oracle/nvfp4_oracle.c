@@ -294,15 +294,19 @@ int oracle_gemv_exact(const uint8_t* a, const uint8_t* b, const uint8_t* sfa, co
  *
  *   ((l*rest_m + m/128)*rest_k + kb/4)*512 + (m%32)*16 + ((m/32)%4)*4 + kb%4
  *
- * Rows m in [rows, 128*rest_m) are padding and hold 0x00.  Requires K%64==0.
+ * with rest_m = ceil(rows/128) and rest_k = ceil(K/64): both helpers size the
+ * blocked tensor with ceil_div (rows/128, (K/16)/4).  Rows m in
+ * [rows, 128*rest_m) and, when K % 64 != 0, blocks kb in [K/16, 4*rest_k) are
+ * padding and hold 0x00 (the pages fill neither; zero is the plainest reading,
+ * and a zero scale adds nothing to any dot product).
  */
 int64_t oracle_permuted_scale_bytes(int64_t rows, int64_t K, int64_t L) {
-  int64_t rest_m = (rows + 127) / 128, rest_k = K / 64;
+  int64_t rest_m = (rows + 127) / 128, rest_k = (K + 63) / 64;
   return L * rest_m * rest_k * 512;
 }
 
 void oracle_repack_scales(const uint8_t* src, uint8_t* dst, int64_t rows, int64_t K, int64_t L) {
-  const int64_t blocks = K / 16, rest_m = (rows + 127) / 128, rest_k = K / 64;
+  const int64_t blocks = K / 16, rest_m = (rows + 127) / 128, rest_k = (K + 63) / 64;
   memset(dst, 0, (size_t)oracle_permuted_scale_bytes(rows, K, L));
   for (int64_t l = 0; l < L; ++l)
     for (int64_t m = 0; m < rows; ++m)

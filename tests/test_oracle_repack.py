@@ -27,6 +27,15 @@ def blocked_per_batch_torch(src):
     return blocks.reshape(-1, 4, 32, 4).transpose(1, 2).reshape(-1, 32, 16).flatten()
 
 
+def blocked_per_batch_padded_torch(src):
+    """to_blocked_batch on a slice first padded with zero rows/columns up to the
+    ceil_div sizes it computes (its view needs whole 128x4 atoms)."""
+    rows, cols = src.shape
+    padded = torch.zeros((rows + 127) // 128 * 128, (cols + 3) // 4 * 4, dtype=src.dtype)
+    padded[:rows, :cols] = src
+    return blocked_per_batch_torch(padded)
+
+
 def blocked_index_math_numpy(src_l, rows, cols):
     """Restatement of submission 69575's scatter indices (output sized for padding)."""
     ncb = (cols + 3) // 4
@@ -54,8 +63,21 @@ def test_repack_equals_to_blocked_batch(rows, K, L):
         assert np.array_equal(got[l], want)
 
 
+@pytest.mark.parametrize("rows,K,L", [(130, 80, 2), (1, 16, 1), (300, 1072, 1), (128, 112, 3)])
+def test_repack_equals_padded_to_blocked_batch(rows, K, L):
+    rng = np.random.default_rng(rows + 3 * K)
+    src = rng.integers(0, 256, (L, rows, K // 16), dtype=np.uint8)
+    got = oracle.repack_scales(src, rows, K, L).reshape(L, -1)
+    for l in range(L):
+        want = blocked_per_batch_padded_torch(torch.from_numpy(src[l].copy())).numpy()
+        assert np.array_equal(got[l], want)
+
+
 @pytest.mark.parametrize("rows,K,L", [(1, 64, 1), (1, 256, 3), (31, 128, 2), (129, 64, 1),
-                                      (200, 320, 2), (128, 64, 2), (7, 1024, 1)])
+                                      (200, 320, 2), (128, 64, 2), (7, 1024, 1),
+                                      # K % 64 != 0: a partly padded last atom column
+                                      (1, 16, 2), (33, 48, 1), (130, 80, 2), (5, 1040, 1),
+                                      (256, 208, 1)])
 def test_repack_equals_index_math_with_zero_padding(rows, K, L):
     rng = np.random.default_rng(rows * 7 + K)
     src = rng.integers(1, 256, (L, rows, K // 16), dtype=np.uint8)  # no zero source bytes
@@ -65,7 +87,8 @@ def test_repack_equals_index_math_with_zero_padding(rows, K, L):
         assert np.array_equal(got[l], want)
     # every source byte appears once; everything else is 0x00 padding
     assert np.count_nonzero(got) == src.size
-    assert oracle.permuted_scale_bytes(rows, K, L) == L * ((rows + 127) // 128) * (K // 64) * 512
+    assert oracle.permuted_scale_bytes(rows, K, L) == \
+        L * ((rows + 127) // 128) * ((K + 63) // 64) * 512
 
 
 @pytest.mark.parametrize("rows,K,L", [(256, 256, 2), (130, 128, 3)])
