@@ -26,7 +26,10 @@
  *        rest_k, L] of submission 103289 (`permuted_to_blocked`), stored
  *        L-outermost in 128x4 atoms of 512 bytes: byte (m, kb) of batch l is
  *        at ((l*rest_m + m/128)*rest_k + kb/4)*512 + (m%32)*16
- *        + ((m/32)%4)*4 + kb%4, rest_m = ceil(rows/128), rest_k = K/64.
+ *        + ((m/32)%4)*4 + kb%4, rest_m = ceil(rows/128), rest_k = ceil(K/64)
+ *        (both sized with ceil_div as in submission 69953's
+ *        `to_blocked_batch`; padding rows and, when K % 64 != 0, the padding
+ *        blocks of the last atom column hold 0x00).
  *        For sfb, rows = 1 (row 0 of each atom is used).
  *        nvfp4_repack_scales() produces this layout from the plain one.
  *
@@ -62,7 +65,8 @@ typedef enum {
 typedef enum {
   NVFP4_OK = 0,
   NVFP4_ERR_INVALID_VALUE = 1,     /* NULL pointer with non-empty data, negative size, bad enum */
-  NVFP4_ERR_UNSUPPORTED_SHAPE = 2, /* K % 64 != 0, or a size beyond the limits below */
+  NVFP4_ERR_UNSUPPORTED_SHAPE = 2, /* K % 16 != 0, a size beyond the limits below, or a
+                                      shape the selected kernel cannot run */
   NVFP4_ERR_MISALIGNED = 3,        /* pointer alignment rule broken (see each call) */
   NVFP4_ERR_CUDA = 4               /* a CUDA runtime call failed; see nvfp4_last_cuda_error() */
 } nvfp4_status_t;
@@ -76,11 +80,15 @@ typedef enum {
  *   sf_layout      : NVFP4_SF_PLAIN or NVFP4_SF_PERMUTED_128x4
  *   stream         : CUDA stream (cudaStream_t)
  *
- * Shapes: M, L >= 0 and K >= 0 with K % 64 == 0 (the pages' K tile and
- * scale atom, `mma_tiler_mnk = (128, 1, 64)`).  M == 0 or L == 0 is a no-op
+ * Shapes: M, L >= 0 and K >= 0 with K % 16 == 0 (whole 16-element scale
+ * blocks; the pages' kernels take K % 64 == 0, their K tile and scale atom
+ * `mma_tiler_mnk = (128, 1, 64)`, and K % 64 != 0 runs on the blockwise
+ * kernel).  M == 0 or L == 0 is a no-op
  * (pointers may be NULL).  K == 0 writes +0 to every c (a, b, sfa, sfb may be
  * NULL).  Limits: K <= 2^30, M*L < 2^40.
- * Alignment: a, b, sfa, sfb 32-byte aligned; c 2-byte aligned.
+ * Alignment: a and b 16-byte aligned, sfa and sfb 32-byte aligned (the
+ * pages' `assumed_align` of 16 and 32), c 2-byte aligned.  (A 16-byte
+ * aligned a is never run on the direct kernel, whose 256-bit loads need 32.)
  * Accuracy: on the CUDA-core kernels each 16-element block's dot product is
  * exact and blocks are scaled and summed in FP32 (nvfp4_gemv always runs one
  * of them).
@@ -111,11 +119,11 @@ nvfp4_status_t nvfp4_gemv(const void* a, const void* b, const void* sfa, const v
  *                      addition are one fp32 fused multiply-add before the fp16
  *                      rounding.
  *   b_batch_stride   : bytes from batch l to batch l+1 of b; 0 = K/2 (dense).
- *                      Otherwise >= K/2 and a multiple of 32: b may be row 0 of
+ *                      Otherwise >= K/2 and a multiple of 16: b may be row 0 of
  *                      an N-padded [L][N][K/2] buffer such as the one
  *                      submission 103289's host code builds (stride N*K/2).
  *   sfb_batch_stride : bytes from batch l to batch l+1 of sfb; 0 = dense
- *                      (K/16 plain, (K/64)*512 permuted).  Otherwise at least
+ *                      (K/16 plain, ceil(K/64)*512 permuted).  Otherwise at least
  *                      that, and a multiple of 4 (plain) or 16 (permuted).
  * Violations: a stride below the dense size -> NVFP4_ERR_INVALID_VALUE; a
  * stride or bias pointer off its alignment -> NVFP4_ERR_MISALIGNED.
@@ -138,7 +146,7 @@ nvfp4_status_t nvfp4_gemv_ex(const void* a, const void* b, const void* sfa, cons
 /* The GEMV kernels (CUDA-core kernels 0 and 1 share their arithmetic). */
 typedef enum {
   /* Warps load up to 8 rows' 32-byte K chunks straight into registers with
-   * 256-bit loads, then compute. */
+   * 256-bit loads, then compute.  Needs a 32-byte aligned a. */
   NVFP4_KERNEL_DIRECT = 0,
   /* Each lane copies its rows' chunks and scale words into a 3-slot
    * per-warp shared-memory ring with cp.async, so every warp keeps two tasks
@@ -172,7 +180,15 @@ typedef enum {
    * depth and scale layout).  k_split must be 1.  Plain scales need
    * K % 256 == 0.  Selected explicitly only: measured on GB300 it matches the
    * pipelined kernel on the largest streams and is slower on smaller ones. */
-  NVFP4_KERNEL_BLOCKDOT = 3
+  NVFP4_KERNEL_BLOCKDOT = 3,
+  /* CUDA cores, any K % 16 == 0: each warp takes a group of 4 rows, each lane
+   * whole 16-element blocks (8 bytes of a row of A, one aligned load whatever
+   * K % 64 is), b's block decoded once for the 4 rows, then a shuffle sum over
+   * the lanes.  Block arithmetic as in kernels 0 and 1; the fp32 sums run in
+   * an order fixed by K alone.  lanes_per_row must be 32 and k_split 1.
+   * nvfp4_gemv runs it for K % 64 != 0; the other kernels need K % 64 == 0
+   * (NVFP4_ERR_UNSUPPORTED_SHAPE otherwise). */
+  NVFP4_KERNEL_BLOCKWISE = 4
 } nvfp4_kernel_t;
 
 /*
@@ -207,8 +223,9 @@ nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa
  * N = 1 is nvfp4_gemv_ex with permuted scales (the CUDA-core GEMV); N >= 2
  * runs the tensor-core kernel (NVFP4_KERNEL_TENSOR), whose cost does not grow
  * with N.  Shapes: M, L >= 0, 0 <= N <= 16 (N > 16: UNSUPPORTED_SHAPE),
- * K % 64 == 0 (K = 0 gives c = fp16(bias) or zeros).  Alignment: a, b, sfa,
- * sfb 32 bytes; c and bias 2 bytes; batch strides as for nvfp4_gemv_ex.
+ * K % 64 == 0 (K = 0 gives c = fp16(bias) or zeros).  Alignment: a and b
+ * 16 bytes, sfa and sfb 32 bytes; c and bias 2 bytes; batch strides as for
+ * nvfp4_gemv_ex.
  */
 nvfp4_status_t nvfp4_gemm_small_n(const void* a, const void* b, const void* sfa, const void* sfb,
                                   void* c, int64_t M, int64_t N, int64_t K, int64_t L,
@@ -240,18 +257,19 @@ nvfp4_status_t nvfp4_gemm_small_n_plan(int64_t M, int64_t N, int64_t K, int64_t 
  * Scale repack: plain [L][rows][K/16] E4M3 -> the 128x4-atom pre-permuted
  * layout above (submission 69953, `to_blocked_batch`; submission 69575,
  * `blocked_transform_kernel`).  A byte permutation, bit-exact; padding rows
- * rows..128*rest_m-1 of the last atom row are written as 0x00.  dst must hold
+ * rows..128*rest_m-1 of the last atom row, and blocks K/16..4*rest_k-1 of the
+ * last atom column when K % 64 != 0, are written as 0x00.  dst must hold
  * nvfp4_permuted_scale_bytes(rows, K, L) bytes and must not overlap src.
  * Use rows = M for sfa and rows = 1 for sfb.
- * Shapes: rows, L >= 0, K % 64 == 0 (empty is a no-op).
+ * Shapes: rows, L >= 0, K % 16 == 0 (empty is a no-op).
  * Alignment: src 4-byte aligned; dst 16-byte aligned.  With K % 256 == 0 and a
  * 16-byte aligned src a shared-memory-free kernel runs; the result is the same.
  */
 nvfp4_status_t nvfp4_repack_scales(const void* src, void* dst, int64_t rows, int64_t K,
                                    int64_t L, struct CUstream_st* stream);
 
-/* Bytes of a permuted scale tensor: L * ceil(rows/128) * (K/64) * 512.
- * Returns 0 for invalid arguments (negative sizes or K % 64 != 0). */
+/* Bytes of a permuted scale tensor: L * ceil(rows/128) * ceil(K/64) * 512.
+ * Returns 0 for invalid arguments (negative sizes or K % 16 != 0). */
 size_t nvfp4_permuted_scale_bytes(int64_t rows, int64_t K, int64_t L);
 
 /* Static, human-readable name of a status code. */
@@ -274,9 +292,9 @@ int nvfp4_tensor_wait_timeouts(int reset);
  * nvfp4_kernel_t value that kernel's plan (NVFP4_ERR_UNSUPPORTED_SHAPE if it
  * cannot run the shape).  num_sms is the device's multiprocessor count and
  * ctas_per_sm the number of the CUDA-core kernel's CTAs resident per SM (pass
- * 0 to use the compiled-in default of 2).  nvfp4_gemv picks: the direct
- * kernel for K = 0 and for plain scales up to 512 KB of A; the pipelined
- * kernel otherwise.  For the tensor-core kernel the plan assumes 4 resident
+ * 0 to use the compiled-in default of 2).  nvfp4_gemv picks: the blockwise
+ * kernel for K % 64 != 0; the direct kernel for K = 0 and for plain scales up
+ * to 512 KB of A; the pipelined kernel otherwise.  For the tensor-core kernel the plan assumes 4 resident
  * CTAs per SM (a launch recomputes its grid from the device's limits); for
  * the block-dot kernel, one CTA per SM and up to 227 KB of shared memory.
  */
@@ -284,17 +302,18 @@ typedef struct {
   int kernel;         /* nvfp4_kernel_t */
   int lanes_per_row;  /* lanes of a warp that share one row (32-byte K chunk
                          each); tensor-core kernel: pipeline stages per CTA;
-                         block-dot kernel: ring slots */
+                         block-dot kernel: ring slots; blockwise: 32 */
   int k_split;        /* warps of a CTA that split one row's K range;
                          tensor-core kernel: CTAs per cluster; block-dot: 1 */
   int rows_per_pass;  /* rows a warp reduces at once; tensor-core and
-                         block-dot kernels: 128 (a tile) */
+                         block-dot kernels: 128 (a tile); blockwise: rows a
+                         CTA takes at once (8 warps x 4) */
   int threads_per_cta;
   int64_t ctas;       /* grid size */
   int64_t steps;      /* K chunks per lane per row, ceil(K/64 / lanes_per_row);
                          tensor-core kernel: 256-element K stages, ceil(K/256);
                          block-dot kernel: ceil(K/512) (ceil(K/256) when
-                         K % 256 != 0) */
+                         K % 256 != 0); blockwise: ceil(K/16 / 32) */
 } nvfp4_gemv_plan_t;
 
 nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, int kernel,

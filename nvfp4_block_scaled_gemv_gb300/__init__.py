@@ -60,6 +60,7 @@ KERNEL_DIRECT = 0
 KERNEL_PIPELINED = 1
 KERNEL_TENSOR = 2
 KERNEL_BLOCKDOT = 3
+KERNEL_BLOCKWISE = 4
 
 
 class _Plan(ctypes.Structure):
@@ -220,6 +221,16 @@ def _stream_handle(stream, device) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _on_device(device):
+    """Makes `device` current for a call (the library plans and launches on the
+    calling thread's current device)."""
+    import contextlib
+
+    import torch
+
+    return torch.cuda.device(device) if device.type == "cuda" else contextlib.nullcontext()
+
+
 def _need(t, name, dtype, numel, device):
     import torch
 
@@ -256,8 +267,9 @@ def gemv(a, b, sfa, sfb, c=None, sf_layout: int = SF_PLAIN, stream=None):
     if c is None:
         c = torch.empty((L, M), dtype=torch.float16, device=dev)
     _need(c, "c", torch.float16, L * M, dev)
-    nvfp4_gemv(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(), c.data_ptr(), M, K, L,
-               sf_layout, _stream_handle(stream, dev))
+    with _on_device(dev):
+        nvfp4_gemv(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(), c.data_ptr(), M, K,
+                   L, sf_layout, _stream_handle(stream, dev))
     return c
 
 
@@ -274,6 +286,7 @@ def repack_scales(src, dst=None, stream=None):
     if dst is None:
         dst = torch.empty(n, dtype=torch.uint8, device=src.device)
     _need(dst, "dst", torch.uint8, n, src.device)
-    nvfp4_repack_scales(src.data_ptr(), dst.data_ptr(), rows, K, L,
-                        _stream_handle(stream, src.device))
+    with _on_device(src.device):
+        nvfp4_repack_scales(src.data_ptr(), dst.data_ptr(), rows, K, L,
+                            _stream_handle(stream, src.device))
     return dst

@@ -1,4 +1,5 @@
 // C ABI: argument validation, launch planning and dispatch.
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 
@@ -65,19 +66,22 @@ nvfp4_status_t validate_gemv_shape(int64_t M, int64_t K, int64_t L, int sf_layou
   if (M < 0 || K < 0 || L < 0) return NVFP4_ERR_INVALID_VALUE;
   if (sf_layout != NVFP4_SF_PLAIN && sf_layout != NVFP4_SF_PERMUTED_128x4)
     return NVFP4_ERR_INVALID_VALUE;
-  if (K % 64 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (K % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (K > kMaxK || M > kMaxM) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (M != 0 && L > kMaxRows / M) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   return NVFP4_OK;
 }
 
+// a and b 16-byte aligned (submission 103289's `assumed_align=16`), the
+// scales 32-byte aligned (its `assumed_align=32`), c 2-byte aligned.  The
+// direct kernel's 256-bit loads of a also need a 32-byte aligned a.
 nvfp4_status_t validate_gemv_pointers(const void* a, const void* b, const void* sfa,
                                       const void* sfb, const void* c, int64_t K) {
   if (c == nullptr) return NVFP4_ERR_INVALID_VALUE;
   if (K > 0 && (a == nullptr || b == nullptr || sfa == nullptr || sfb == nullptr))
     return NVFP4_ERR_INVALID_VALUE;
   if (!aligned(c, 2)) return NVFP4_ERR_MISALIGNED;
-  if (K > 0 && (!aligned(a, 32) || !aligned(b, 32) || !aligned(sfa, 32) || !aligned(sfb, 32)))
+  if (K > 0 && (!aligned(a, 16) || !aligned(b, 16) || !aligned(sfa, 32) || !aligned(sfb, 32)))
     return NVFP4_ERR_MISALIGNED;
   return NVFP4_OK;
 }
@@ -90,9 +94,9 @@ const nvfp4_gemv_options_t kDefaultOptions = {1.0f, nullptr, 0, 0};
 nvfp4_status_t validate_options(const nvfp4_gemv_options_t& o, int64_t K, int sf_layout) {
   if (o.b_batch_stride < 0 || o.sfb_batch_stride < 0) return NVFP4_ERR_INVALID_VALUE;
   if (o.b_batch_stride != 0 && o.b_batch_stride < K / 2) return NVFP4_ERR_INVALID_VALUE;
-  if (o.b_batch_stride % 32 != 0) return NVFP4_ERR_MISALIGNED;
+  if (o.b_batch_stride % 16 != 0) return NVFP4_ERR_MISALIGNED;
   const bool permuted = sf_layout == NVFP4_SF_PERMUTED_128x4;
-  const int64_t sfb_dense = permuted ? (K / 64) * 512 : K / 16;
+  const int64_t sfb_dense = permuted ? (K + 63) / 64 * 512 : K / 16;
   if (o.sfb_batch_stride != 0 && o.sfb_batch_stride < sfb_dense) return NVFP4_ERR_INVALID_VALUE;
   if (o.sfb_batch_stride % (permuted ? 16 : 4) != 0) return NVFP4_ERR_MISALIGNED;
   if (o.bias != nullptr && !aligned(o.bias, 2)) return NVFP4_ERR_MISALIGNED;
@@ -110,7 +114,7 @@ GemvParams make_params(const void* a, const void* b, const void* sfa, const void
   p.c = static_cast<uint16_t*>(c);
   p.M = M;
   p.rest_m = (int32_t)((M + 127) / 128);
-  p.rest_k = (int32_t)(K / 64);
+  p.rest_k = (int32_t)((K + 63) / 64);
   p.rows_per_l = permuted ? (int64_t)p.rest_m * 128 : M;
   p.rows_total = p.rows_per_l * L;
   p.half_k = (int32_t)(K / 2);
@@ -144,7 +148,9 @@ nvfp4_status_t run_gemv(const void* a, const void* b, const void* sfa, const voi
   const bool permuted = sf_layout == NVFP4_SF_PERMUTED_128x4;
   const GemvParams p = make_params(a, b, sfa, sfb, c, M, K, L, permuted, plan, opt);
   cudaError_t err;
-  if (plan.kernel == kKernelBlockDot)
+  if (plan.kernel == kKernelBlockwise)
+    err = launch_gemv_blockwise(p, permuted, plan.ctas, stream);
+  else if (plan.kernel == kKernelBlockDot)
     err = launch_blockdot(p, permuted, L, plan.lanes_per_row, plan.ctas, stream);
   else if (plan.kernel == kKernelTensor)
     err = launch_gemv_tc(p, 1, L, K / 2, plan.lanes_per_row, plan.k_split, plan.ctas, stream);
@@ -253,13 +259,13 @@ nvfp4_status_t validate_gemm(const void* a, const void* b, const void* sfa, cons
   if (o.b_batch_stride < 0 || o.sfb_batch_stride < 0) return NVFP4_ERR_INVALID_VALUE;
   if (o.b_batch_stride != 0 && o.b_batch_stride < N * (K / 2)) return NVFP4_ERR_INVALID_VALUE;
   if (o.sfb_batch_stride != 0 && o.sfb_batch_stride < (K / 64) * 512) return NVFP4_ERR_INVALID_VALUE;
-  if (o.b_batch_stride % 32 != 0 || o.sfb_batch_stride % 16 != 0) return NVFP4_ERR_MISALIGNED;
+  if (o.b_batch_stride % 16 != 0 || o.sfb_batch_stride % 16 != 0) return NVFP4_ERR_MISALIGNED;
   if (M == 0 || N == 0 || L == 0) return NVFP4_OK;
   if (c == nullptr) return NVFP4_ERR_INVALID_VALUE;
   if (K > 0 && (a == nullptr || b == nullptr || sfa == nullptr || sfb == nullptr))
     return NVFP4_ERR_INVALID_VALUE;
   if (!aligned(c, 2) || (o.bias != nullptr && !aligned(o.bias, 2))) return NVFP4_ERR_MISALIGNED;
-  if (K > 0 && (!aligned(a, 32) || !aligned(b, 32) || !aligned(sfa, 32) || !aligned(sfb, 32)))
+  if (K > 0 && (!aligned(a, 16) || !aligned(b, 16) || !aligned(sfa, 32) || !aligned(sfb, 32)))
     return NVFP4_ERR_MISALIGNED;
   return NVFP4_OK;
 }
@@ -286,6 +292,7 @@ nvfp4_status_t run_gemm_tc(const void* a, const void* b, const void* sfa, const 
 
 int rows_per_pass(const GemvPlan& plan) {
   if (plan.kernel == kKernelTensor || plan.kernel == kKernelBlockDot) return 128;  // a tile of A rows
+  if (plan.kernel == kKernelBlockwise) return kBlockwiseRows * kGemvWarps;
   return plan.kernel == kKernelAsync ? kAsyncItems * (32 / plan.lanes_per_row) * plan.groups
                                      : kRowsPerPass;
 }
@@ -367,8 +374,22 @@ int async_groups(int64_t M, int64_t L, bool permuted, int lanes_per_row, int k_s
 bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int num_sms,
                int ctas_per_sm, GemvPlan* out) {
   if (M < 0 || K < 0 || L < 0 || num_sms < 1 || ctas_per_sm < 1 || out == nullptr) return false;
-  if (kernel < -1 || kernel > kKernelBlockDot) return false;
+  if (kernel < -1 || kernel > kKernelBlockwise) return false;
   const int64_t kchunks = K / 64;
+  // K % 64 != 0 (K a multiple of 16): the blockwise kernel alone runs it
+  if (kernel == -1 && K % 64 != 0) kernel = kKernelBlockwise;
+  if (kernel == kKernelBlockwise) {
+    const int64_t groups = L * ((M + kBlockwiseRows - 1) / kBlockwiseRows);
+    const int64_t warps = (int64_t)num_sms * ctas_per_sm * kGemvWarps;
+    out->kernel = kKernelBlockwise;
+    out->lanes_per_row = 32;
+    out->k_split = 1;
+    out->groups = 1;
+    out->ctas = std::max<int64_t>(1, (std::min(groups, warps) + kGemvWarps - 1) / kGemvWarps);
+    out->steps = (K / 16 + 31) / 32;
+    return true;
+  }
+  if (K % 64 != 0) return false;
   const int64_t a_bytes = M * L * (K / 2);
   // Tiny problems with plain scales (measured on GB300 over 16 KB .. 2 MB of
   // A): the launch and the first DRAM access dominate, and fewer, fuller CTAs
@@ -518,6 +539,11 @@ nvfp4_status_t nvfp4_gemv_ex(const void* a, const void* b, const void* sfa, cons
   GemvPlan plan;
   const bool permuted = sf_layout == NVFP4_SF_PERMUTED_128x4;
   if (!plan_gemv(M, K, L, permuted, -1, sms, occ, &plan)) return NVFP4_ERR_INVALID_VALUE;
+  // the direct kernel loads a with 256-bit loads: a 16-byte aligned a takes
+  // the pipelined kernel (K = 0 reads nothing)
+  if (plan.kernel == kKernelDirect && K > 0 && !aligned(a, 32) &&
+      !plan_gemv(M, K, L, permuted, kKernelAsync, sms, occ, &plan))
+    return NVFP4_ERR_INVALID_VALUE;
   return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, opt, (cudaStream_t)stream);
 }
 
@@ -528,9 +554,28 @@ nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa
   nvfp4_status_t st = validate_gemv_shape(M, K, L, sf_layout);
   if (st != NVFP4_OK) return st;
   if (kernel != kKernelDirect && kernel != kKernelAsync && kernel != kKernelTensor &&
-      kernel != kKernelBlockDot)
+      kernel != kKernelBlockDot && kernel != kKernelBlockwise)
     return NVFP4_ERR_INVALID_VALUE;
   const bool permuted = sf_layout == NVFP4_SF_PERMUTED_128x4;
+  if (kernel == kKernelBlockwise) {
+    // 32 lanes per row group, k_split 1
+    if (lanes_per_row != 32 || k_split != 1 || ctas < 1 || ctas > 0x7fffffff)
+      return NVFP4_ERR_INVALID_VALUE;
+    if (M == 0 || L == 0) return NVFP4_OK;
+    st = validate_gemv_pointers(a, b, sfa, sfb, c, K);
+    if (st != NVFP4_OK) return st;
+    GemvPlan plan;
+    plan.kernel = kKernelBlockwise;
+    plan.lanes_per_row = 32;
+    plan.k_split = 1;
+    plan.groups = 1;
+    plan.ctas = ctas;
+    plan.steps = (K / 16 + 31) / 32;
+    return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, kDefaultOptions,
+                    (cudaStream_t)stream);
+  }
+  // the other kernels move 64-element chunks
+  if (K % 64 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (kernel == kKernelBlockDot) {
     // lanes_per_row = ring slots (0: the most that fit), k_split 1
     if (k_split != 1 || ctas < 1 || ctas > 0x7fffffff || lanes_per_row < 0 ||
@@ -574,6 +619,7 @@ nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa
   if (M == 0 || L == 0) return NVFP4_OK;
   st = validate_gemv_pointers(a, b, sfa, sfb, c, K);
   if (st != NVFP4_OK) return st;
+  if (kernel == kKernelDirect && K > 0 && !aligned(a, 32)) return NVFP4_ERR_MISALIGNED;
   GemvPlan plan;
   plan.kernel = kernel;
   plan.lanes_per_row = lanes_per_row;
@@ -591,7 +637,7 @@ nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa
 nvfp4_status_t nvfp4_repack_scales(const void* src, void* dst, int64_t rows, int64_t K,
                                    int64_t L, struct CUstream_st* stream) {
   if (rows < 0 || K < 0 || L < 0) return NVFP4_ERR_INVALID_VALUE;
-  if (K % 64 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (K % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (K > kMaxK || rows > kMaxM) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (rows != 0 && L > kMaxRows / rows) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (rows == 0 || K == 0 || L == 0) return NVFP4_OK;
@@ -607,8 +653,8 @@ nvfp4_status_t nvfp4_repack_scales(const void* src, void* dst, int64_t rows, int
 }
 
 size_t nvfp4_permuted_scale_bytes(int64_t rows, int64_t K, int64_t L) {
-  if (rows < 0 || K < 0 || L < 0 || K % 64 != 0) return 0;
-  return (size_t)(L * ((rows + 127) / 128) * (K / 64) * 512);
+  if (rows < 0 || K < 0 || L < 0 || K % 16 != 0) return 0;
+  return (size_t)(L * ((rows + 127) / 128) * ((K + 63) / 64) * 512);
 }
 
 const char* nvfp4_status_string(int status) {
@@ -687,7 +733,7 @@ nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, i
   nvfp4_status_t st = validate_gemv_shape(M, K, L, sf_layout);
   if (st != NVFP4_OK) return st;
   GemvPlan plan;
-  if (kernel < -1 || kernel > kKernelBlockDot) return NVFP4_ERR_INVALID_VALUE;
+  if (kernel < -1 || kernel > kKernelBlockwise) return NVFP4_ERR_INVALID_VALUE;
   if (!plan_gemv(M, K, L, sf_layout == NVFP4_SF_PERMUTED_128x4, kernel, num_sms,
                  ctas_per_sm > 0 ? ctas_per_sm : kGemvMinCtasPerSm, &plan))
     return NVFP4_ERR_UNSUPPORTED_SHAPE;

@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
   };
   auto load_b = [&](int l, int kt, uint32_t (&w)[8], uint32_t& sw) {
     if (kt < p.kchunks) {
-      ld_shared_256(p.b + (int64_t)l * p.b_stride + kt * 32, w);
+      ld_shared_2x128(p.b + (int64_t)l * p.b_stride + kt * 32, w);
       sw = ld_scale_32(p.sfb + (int64_t)l * p.sfb_stride + (PERM ? (int64_t)kt * 512 : kt * 4));
     }
   };

@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kGemvThreads, kGemvMinCtasPerSm)
           }
         }
         uint32_t bw[8];
-        ld_shared_256(brow + (int64_t)kt * 32, bw);
+        ld_shared_2x128(brow + (int64_t)kt * 32, bw);
         const uint32_t sbw = ld_scale_32(sbrow + kt * scale_chunk_stride<PERM>());
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {

@@ -19,7 +19,13 @@ constexpr int kAsyncStages = 3;
 constexpr int kAsyncStageBytes = kAsyncItems * (32 * 32 + 32 * 4);
 constexpr int kAsyncSmemBytes = kGemvWarps * kAsyncStages * kAsyncStageBytes;
 
-enum KernelKind { kKernelDirect = 0, kKernelAsync = 1, kKernelTensor = 2, kKernelBlockDot = 3 };
+enum KernelKind {
+  kKernelDirect = 0,
+  kKernelAsync = 1,
+  kKernelTensor = 2,
+  kKernelBlockDot = 3,
+  kKernelBlockwise = 4
+};
 
 // Everything a GEMV kernel needs, by value (kernel parameter space).
 struct GemvParams {
@@ -43,7 +49,7 @@ struct GemvParams {
   int32_t kchunks;    // K/64: 32-byte chunks per row (one per 128x4 atom column)
   int32_t steps;      // ceil(kchunks / lanes_per_row)
   int32_t rest_m;     // ceil(M/128)
-  int32_t rest_k;     // K/64
+  int32_t rest_k;     // ceil(K/64): atom columns of a pre-permuted row
 };
 
 struct GemvPlan {
@@ -73,6 +79,8 @@ cudaError_t gemv_ctas_per_sm(int* out);
 
 // Scale repack: occupancy (CTAs per SM) and launch over at most max_ctas CTAs.
 cudaError_t repack_ctas_per_sm(int* out);
+// Any K % 16 == 0: the last atom column of a K % 64 != 0 repack is padded
+// with 0x00.
 cudaError_t launch_repack(const uint8_t* src, uint8_t* dst, int64_t rows, int64_t K, int64_t L,
                           int64_t max_ctas, cudaStream_t stream);
 
@@ -109,6 +117,13 @@ int blockdot_max_stages(bool permuted, int column_blocks, int slot_rows, size_t 
 cudaError_t launch_blockdot(const GemvParams& p, bool permuted, int64_t L, int stages,
                             int64_t ctas, cudaStream_t stream);
 cudaError_t blockdot_wait_timeouts(int reset, int* out);
+
+// Blockwise kernel (gemv_blockwise.cu): one 16-element block per lane and
+// step, any K % 16 == 0; groups of kBlockwiseRows rows over the grid's warps
+// (kGemvThreads threads per CTA).
+constexpr int kBlockwiseRows = 4;
+cudaError_t launch_gemv_blockwise(const GemvParams& p, bool permuted, int64_t ctas,
+                                  cudaStream_t stream);
 
 // Per-layout GEMV launchers (gemv_plain.cu, gemv_permuted.cu).
 cudaError_t launch_gemv_plain(const GemvParams& p, const GemvPlan& plan, cudaStream_t stream);

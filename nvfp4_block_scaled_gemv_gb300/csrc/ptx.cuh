@@ -15,9 +15,11 @@ __device__ __forceinline__ void ld_stream_256(const void* p, uint32_t (&r)[8]) {
       : "l"(p));
 }
 
-// 256-bit load of data many warps re-read (the vector b): normal L1 caching.
-__device__ __forceinline__ void ld_shared_256(const void* p, uint32_t (&r)[8]) {
-  asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+// 32 bytes of data many warps re-read (the vector b) as two 128-bit loads
+// with normal L1 caching (b needs only 16-byte alignment).
+__device__ __forceinline__ void ld_shared_2x128(const void* p, uint32_t (&r)[8]) {
+  asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%8];\n\t"
+               "ld.global.nc.v4.b32 {%4,%5,%6,%7}, [%8+16];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
                  "=r"(r[6]), "=r"(r[7])
                : "l"(p));

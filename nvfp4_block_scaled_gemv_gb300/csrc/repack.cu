@@ -101,6 +101,34 @@ __global__ void __launch_bounds__(kVecThreads)
   out[96] = make_uint4(x[0].w, x[1].w, x[2].w, x[3].w);
 }
 
+// Any K % 16 == 0 (plain rows K/16 bytes long, not always 4-byte aligned):
+// thread w writes the w-th 4-byte word of the output, gathering its 4 scale
+// bytes (blocks past K/16 and rows past `rows` are 0x00).
+__global__ void __launch_bounds__(kRepackThreads)
+    repack_scales_bytes_kernel(const uint8_t* __restrict__ src, uint32_t* __restrict__ dst,
+                               int64_t rows, int64_t blocks, int32_t rest_m, int32_t rest_k,
+                               int64_t words) {
+  for (int64_t w = (int64_t)blockIdx.x * kRepackThreads + threadIdx.x; w < words;
+       w += (int64_t)gridDim.x * kRepackThreads) {
+    const int64_t atom = w / 128;              // (l*rest_m + m/128)*rest_k + kc
+    const int in_atom = (int)(w % 128);        // i*4 + g: row 32*g + i of the block
+    const int i = in_atom / 4, g = in_atom % 4;
+    const int64_t kc = atom % rest_k, blk = atom / rest_k;  // blk = l*rest_m + m/128
+    const int64_t l = blk / rest_m;
+    const int64_t m = (blk - l * rest_m) * 128 + 32 * g + i;
+    uint32_t v = 0;
+    if (m < rows) {
+      const uint8_t* row = src + (l * rows + m) * blocks;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int64_t kb = 4 * kc + t;
+        if (kb < blocks) v |= (uint32_t)row[kb] << (8 * t);
+      }
+    }
+    dst[w] = v;
+  }
+}
+
 }  // namespace
 
 cudaError_t repack_ctas_per_sm(int* out) {
@@ -111,7 +139,20 @@ cudaError_t repack_ctas_per_sm(int* out) {
 cudaError_t launch_repack(const uint8_t* src, uint8_t* dst, int64_t rows, int64_t K, int64_t L,
                           int64_t max_ctas, cudaStream_t stream) {
   const int32_t rest_m = (int32_t)((rows + 127) / 128);
-  const int32_t rest_k = (int32_t)(K / 64);
+  const int32_t rest_k = (int32_t)((K + 63) / 64);
+  if (K % 64 != 0) {
+    const int64_t words = L * rest_m * (int64_t)rest_k * 128;
+    if (words == 0) return cudaSuccess;
+    const int64_t cap = max_ctas > 0 ? max_ctas : 1;
+    const int64_t need = (words + kRepackThreads - 1) / kRepackThreads;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(need < cap ? need : cap), 1, 1);
+    cfg.blockDim = dim3(kRepackThreads, 1, 1);
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, repack_scales_bytes_kernel, src,
+                              reinterpret_cast<uint32_t*>(dst), rows, K / 16, rest_m, rest_k,
+                              words);
+  }
   const int32_t qw = rest_k / 4;
   const int64_t units = L * rest_m * 32 * (int64_t)((qw + 3) / 4) * 4;
   if (rest_k % 4 == 0 && reinterpret_cast<uintptr_t>(src) % 16 == 0 &&

@@ -59,16 +59,17 @@ def test_validation_before_any_cuda_call(lib):
     assert _call(lib, K=-64) == nv.ERR_INVALID_VALUE
     assert _call(lib, L=-2) == nv.ERR_INVALID_VALUE
     assert _call(lib, layout=2) == nv.ERR_INVALID_VALUE
-    assert _call(lib, K=96) == nv.ERR_UNSUPPORTED_SHAPE
+    assert _call(lib, K=88) == nv.ERR_UNSUPPORTED_SHAPE  # whole 16-element blocks only
     assert _call(lib, K=(1 << 30) + 64) == nv.ERR_UNSUPPORTED_SHAPE
     assert _call(lib, M=1 << 31) == nv.ERR_UNSUPPORTED_SHAPE
     assert _call(lib, M=1 << 30, L=1 << 11) == nv.ERR_UNSUPPORTED_SHAPE
     assert _call(lib, a=None) == nv.ERR_INVALID_VALUE
     assert _call(lib, c=None) == nv.ERR_INVALID_VALUE
     assert _call(lib, sfb=None) == nv.ERR_INVALID_VALUE
-    assert _call(lib, a=64 + 16) == nv.ERR_MISALIGNED
+    # a and b: 16 bytes (the pages' assumed_align=16); scales: 32; c: 2
+    assert _call(lib, a=64 + 8) == nv.ERR_MISALIGNED
     assert _call(lib, b=64 + 8) == nv.ERR_MISALIGNED
-    assert _call(lib, sfa=64 + 4) == nv.ERR_MISALIGNED
+    assert _call(lib, sfa=64 + 16) == nv.ERR_MISALIGNED
     assert _call(lib, sfb=64 + 1) == nv.ERR_MISALIGNED
     assert _call(lib, c=64 + 1) == nv.ERR_MISALIGNED
 
@@ -94,6 +95,39 @@ def test_explicit_schedule_validation(lib):
     assert lib.nvfp4_gemv_explicit(*zero_k, nv.KERNEL_PIPELINED, 32, 1, 1, None) == nv.ERR_INVALID_VALUE
 
 
+def test_k_not_multiple_of_64(lib):
+    """K % 16 == 0 with K % 64 != 0: the blockwise kernel's shapes."""
+    args = (64, 64, 64, 64, 64, 8, 80, 1, 0)
+    for kernel, lpr in ((nv.KERNEL_DIRECT, 32), (nv.KERNEL_PIPELINED, 32), (nv.KERNEL_TENSOR, 4),
+                        (nv.KERNEL_BLOCKDOT, 0)):
+        for layout in (nv.SF_PLAIN, nv.SF_PERMUTED_128x4):
+            assert lib.nvfp4_gemv_explicit(*args[:-1], layout, kernel, lpr, 1, 1, None) == \
+                nv.ERR_UNSUPPORTED_SHAPE
+    B = nv.KERNEL_BLOCKWISE
+    assert lib.nvfp4_gemv_explicit(*args, B, 16, 1, 1, None) == nv.ERR_INVALID_VALUE
+    assert lib.nvfp4_gemv_explicit(*args, B, 32, 2, 1, None) == nv.ERR_INVALID_VALUE
+    assert lib.nvfp4_gemv_explicit(*args, B, 32, 1, 0, None) == nv.ERR_INVALID_VALUE
+    assert lib.nvfp4_gemv_explicit(*(args[:5] + (0,) + args[6:]), B, 32, 1, 1, None) == nv.OK
+    assert lib.nvfp4_gemv_explicit(*(args[:3] + (64 + 16,) + args[4:]), B, 32, 1, 1, None) == \
+        nv.ERR_MISALIGNED
+    for layout in (nv.SF_PLAIN, nv.SF_PERMUTED_128x4):
+        for K in (16, 48, 80, 1040):
+            plan = nv.nvfp4_gemv_plan(4096, K, 8, layout, 152, 2)
+            assert plan["kernel"] == B
+            assert (plan["lanes_per_row"], plan["k_split"], plan["threads_per_cta"]) == (32, 1, 256)
+            assert plan["rows_per_pass"] == 32 and plan["steps"] == (K // 16 + 31) // 32
+            # one warp per 4-row group, at most 2 CTAs per SM
+            assert plan["ctas"] == min(152 * 2, 8 * 1024 // 8)
+        with pytest.raises(nv.Nvfp4Error):
+            nv.nvfp4_gemv_plan(4096, 80, 8, layout, 152, 2, kernel=nv.KERNEL_PIPELINED)
+    # small problems: one warp per group
+    assert nv.nvfp4_gemv_plan(5, 48, 1, 0, 152, 2)["ctas"] == 1
+    assert nv.nvfp4_gemv_plan(100, 48, 3, 0, 152, 2)["ctas"] == (3 * 25 + 7) // 8
+    # K % 64 == 0 keeps its schedule; the blockwise kernel is there on request
+    assert nv.nvfp4_gemv_plan(4096, 1024, 8, 0, 152, 2)["kernel"] == nv.KERNEL_PIPELINED
+    assert nv.nvfp4_gemv_plan(4096, 1024, 8, 0, 152, 2, kernel=B)["kernel"] == B
+
+
 def test_tensor_kernel_schedule_validation(lib):
     # (a, b, sfa, sfb, c, M, K, L, layout): checked before any CUDA call
     perm = (64, 64, 64, 64, 64, 300, 1024, 2, nv.SF_PERMUTED_128x4)
@@ -114,7 +148,7 @@ def test_tensor_kernel_schedule_validation(lib):
 
 def test_repack_validation(lib):
     assert lib.nvfp4_repack_scales(64, 64, -1, 64, 1, None) == nv.ERR_INVALID_VALUE
-    assert lib.nvfp4_repack_scales(64, 64, 4, 80, 1, None) == nv.ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_repack_scales(64, 64, 4, 72, 1, None) == nv.ERR_UNSUPPORTED_SHAPE
     assert lib.nvfp4_repack_scales(None, 64, 4, 64, 1, None) == nv.ERR_INVALID_VALUE
     assert lib.nvfp4_repack_scales(66, 64, 4, 64, 1, None) == nv.ERR_MISALIGNED
     assert lib.nvfp4_repack_scales(64, 72, 4, 64, 1, None) == nv.ERR_MISALIGNED
@@ -124,7 +158,10 @@ def test_permuted_scale_bytes_and_status_strings(lib):
     assert nv.nvfp4_permuted_scale_bytes(7168, 2048, 4) == 4 * 56 * 32 * 512
     assert nv.nvfp4_permuted_scale_bytes(1, 16384, 1) == 256 * 512
     assert nv.nvfp4_permuted_scale_bytes(129, 64, 2) == 2 * 2 * 1 * 512
-    assert nv.nvfp4_permuted_scale_bytes(5, 80, 1) == 0
+    # K % 64 != 0: a last, partly padded atom column
+    assert nv.nvfp4_permuted_scale_bytes(5, 80, 1) == 2 * 512
+    assert nv.nvfp4_permuted_scale_bytes(130, 16, 3) == 3 * 2 * 1 * 512
+    assert nv.nvfp4_permuted_scale_bytes(5, 72, 1) == 0
     assert nv.status_string(nv.OK) == "NVFP4_OK"
     assert nv.status_string(nv.ERR_MISALIGNED) == "NVFP4_ERR_MISALIGNED"
     assert nv.status_string(99) == "NVFP4_ERR_UNKNOWN"
@@ -278,7 +315,7 @@ def test_gemv_ex_option_validation(lib):
 
     assert status(b_batch_stride=-32) == nv.ERR_INVALID_VALUE
     assert status(b_batch_stride=512) == nv.ERR_INVALID_VALUE           # below K/2
-    assert status(b_batch_stride=1024 + 16) == nv.ERR_MISALIGNED         # not a multiple of 32
+    assert status(b_batch_stride=1024 + 8) == nv.ERR_MISALIGNED          # not a multiple of 16
     assert status(sfb_batch_stride=64) == nv.ERR_INVALID_VALUE          # below K/16
     assert status(sfb_batch_stride=130) == nv.ERR_MISALIGNED
     assert status(nv.SF_PERMUTED_128x4, sfb_batch_stride=512) == nv.ERR_INVALID_VALUE  # below 32*512
@@ -459,12 +496,13 @@ def test_gemm_small_n_validation(lib):
     assert G(*ptrs, 300, 4, 1024, 0, None, None) == nv.OK
     assert G(None, 64, 64, 64, 64, 300, 4, 1024, 2, None, None) == nv.ERR_INVALID_VALUE
     assert G(64, 64, 64, 64, None, 300, 4, 1024, 2, None, None) == nv.ERR_INVALID_VALUE
-    assert G(64, 80, 64, 64, 64, 300, 4, 1024, 2, None, None) == nv.ERR_MISALIGNED
+    assert G(64, 72, 64, 64, 64, 300, 4, 1024, 2, None, None) == nv.ERR_MISALIGNED
+    assert G(64, 64, 80, 64, 64, 300, 4, 1024, 2, None, None) == nv.ERR_MISALIGNED
     assert G(64, 64, 64, 64, 65, 300, 4, 1024, 2, None, None) == nv.ERR_MISALIGNED
-    # b batch stride below N*K/2, or not a multiple of 32
+    # b batch stride below N*K/2, or not a multiple of 16
     opt = nv._Options(1.0, None, 4 * 512 - 32, 0)
     assert G(*ptrs, 300, 4, 1024, 2, ctypes.byref(opt), None) == nv.ERR_INVALID_VALUE
-    opt = nv._Options(1.0, None, 4 * 512 + 16, 0)
+    opt = nv._Options(1.0, None, 4 * 512 + 8, 0)
     assert G(*ptrs, 300, 4, 1024, 2, ctypes.byref(opt), None) == nv.ERR_MISALIGNED
     # sfb batch stride below (K/64)*512, or not a multiple of 16
     opt = nv._Options(1.0, None, 0, 16 * 512 - 16)

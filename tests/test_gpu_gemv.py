@@ -213,11 +213,57 @@ def test_misaligned_device_pointers_rejected_without_launch():
     buf = torch.zeros(4096, dtype=torch.uint8, device=DEV)
     c = torch.full((M,), 3.0, dtype=torch.float16, device=DEV)
     base = buf.data_ptr()
+    for ptrs in ((base + 8, base + 1024, base + 2048, base + 3072),
+                 (base, base + 1032, base + 2048, base + 3072),
+                 (base, base + 1024, base + 2064, base + 3072)):
+        with pytest.raises(nv.Nvfp4Error) as e:
+            nv.nvfp4_gemv(*ptrs, c.data_ptr(), M, K, L)
+        assert e.value.status == nv.ERR_MISALIGNED
+    # a direct-kernel schedule needs a 32-byte aligned a
     with pytest.raises(nv.Nvfp4Error) as e:
-        nv.nvfp4_gemv(base + 16, base + 1024, base + 2048, base + 3072, c.data_ptr(), M, K, L)
+        nv.nvfp4_gemv_explicit(base + 16, base + 1024, base + 2048, base + 3072, c.data_ptr(),
+                               M, K, L, nv.SF_PLAIN, nv.KERNEL_DIRECT, 4, 1, 1)
     assert e.value.status == nv.ERR_MISALIGNED
     torch.cuda.synchronize()
     assert np.all(parity.half_values(bits(c)) == 3.0)
+
+
+@pytest.mark.parametrize("layout", [nv.SF_PLAIN, nv.SF_PERMUTED_128x4])
+@pytest.mark.parametrize("M,K,L", [(128, 256, 1), (7, 1024, 3), (1000, 2048, 2), (4096, 4096, 4)])
+def test_sixteen_byte_aligned_a_and_b(M, K, L, layout):
+    """a and b 16 bytes past a 32-byte boundary (the pages' assumed_align=16):
+    the library's own schedule (never the direct kernel for such an a), and
+    every other kernel that runs the shape, against the oracle."""
+    p = synthetic.make_problem(M, K, L, seed=M + 3 * K)
+    ref, sums, sumabs = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
+    abuf = torch.empty(p["a"].size + 64, dtype=torch.uint8, device=DEV)
+    bbuf = torch.empty(p["b"].size + 64, dtype=torch.uint8, device=DEV)
+    a_off, b_off = (16 - abuf.data_ptr()) % 32, (16 - bbuf.data_ptr()) % 32
+    a = abuf[a_off:a_off + p["a"].size]
+    b = bbuf[b_off:b_off + p["b"].size]
+    assert a.data_ptr() % 32 == 16 and b.data_ptr() % 32 == 16
+    a.copy_(torch.from_numpy(p["a"].reshape(-1)))
+    b.copy_(torch.from_numpy(p["b"].reshape(-1)))
+    _, _, sfa, sfb = device_problem(p, M, K, L, layout)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    runs = [None]
+    for kern in (nv.KERNEL_PIPELINED, nv.KERNEL_BLOCKDOT):
+        if kern == nv.KERNEL_BLOCKDOT and layout == nv.SF_PLAIN and K % 256:
+            continue
+        plan = nv.nvfp4_gemv_plan(M, K, L, layout, sms, 0, kernel=kern)
+        runs.append((kern, plan["lanes_per_row"], plan["k_split"], plan["ctas"]))
+    for sched in runs:
+        c = torch.full((L * M,), SENTINEL, dtype=torch.float16, device=DEV)
+        if sched is None:
+            nv.nvfp4_gemv(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(), c.data_ptr(),
+                          M, K, L, layout, torch.cuda.current_stream().cuda_stream)
+        else:
+            nv.nvfp4_gemv_explicit(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(),
+                                   c.data_ptr(), M, K, L, layout, *sched,
+                                   stream=torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        parity.assert_parity(bits(c).reshape(L, M), ref, sums, sumabs,
+                             f"16-byte aligned a, b M={M} K={K} L={L} layout={layout} {sched}")
 
 
 def test_graph_capture_and_replay():
@@ -277,7 +323,8 @@ def test_gemv_ex_defaults_are_nvfp4_gemv(layout):
 
 @pytest.mark.parametrize("layout", [nv.SF_PLAIN, nv.SF_PERMUTED_128x4])
 @pytest.mark.parametrize("M,K,L,alpha", [(700, 2048, 3, 0.375), (129, 7168, 2, -1.5e-3),
-                                         (4096, 1024, 2, 37.0)])
+                                         (4096, 1024, 2, 37.0), (130, 80, 3, -0.75),
+                                         (300, 1040, 2, 3.0)])
 def test_gemv_ex_alpha_bias_and_padded_b(layout, M, K, L, alpha):
     """b as row 0 of an [L][8][K/2] buffer and sfb in a padded per-batch
     stride, the other rows random: only row 0 may reach c."""
@@ -291,13 +338,14 @@ def test_gemv_ex_alpha_bias_and_padded_b(layout, M, K, L, alpha):
     b_pad = torch.from_numpy(rng.integers(0, 256, (L, N, K // 2), dtype=np.uint8)).to(DEV)
     b_pad[:, 0, :] = b.view(L, K // 2)
     sfb_dense = sfb.numel() // L
-    sfb_pad = torch.from_numpy(rng.integers(0, 256, (L, 2 * sfb_dense), dtype=np.uint8)).to(DEV)
+    sfb_stride = -(-2 * sfb_dense // 16) * 16  # a multiple of 16 (of 4 for plain scales)
+    sfb_pad = torch.from_numpy(rng.integers(0, 256, (L, sfb_stride), dtype=np.uint8)).to(DEV)
     sfb_pad[:, :sfb_dense] = sfb.view(L, sfb_dense)
     c = torch.full((L * M,), SENTINEL, dtype=torch.float16, device=DEV)
     bias_d = torch.from_numpy(bias.reshape(-1).copy()).to(DEV)
     got = _ex_call(a, b_pad, sfa, sfb_pad, c, M, K, L, layout, alpha=alpha,
                    bias=bias_d.data_ptr(), b_batch_stride=N * (K // 2),
-                   sfb_batch_stride=2 * sfb_dense)
+                   sfb_batch_stride=sfb_stride)
     parity.assert_parity(got, ref, vals, sumabs, f"ex M={M} K={K} L={L} alpha={alpha} layout={layout}")
 
 
@@ -322,3 +370,70 @@ def test_extreme_shapes(M, K, L, layout):
     ref, sums, sumabs = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
     got = run(p, M, K, L, layout, via_gpu_repack=(layout == nv.SF_PERMUTED_128x4))
     parity.assert_parity(got, ref, sums, sumabs, f"M={M} K={K} L={L} layout={layout}")
+
+
+# --- K % 16 == 0 with K % 64 != 0: the blockwise kernel --------------------
+
+K16_SHAPES = [(1, 16, 1), (7, 48, 2), (130, 80, 3), (33, 1040, 2), (513, 208, 1),
+              (1000, 4112, 2), (4, 16, 300)]
+
+
+@pytest.mark.parametrize("M,K,L", K16_SHAPES)
+def test_k_multiple_of_16(M, K, L):
+    """Every output against the oracle, both layouts (permuted scales through
+    the oracle's and through the GPU's repack, with the padded last atom
+    column), the default plan and explicit grids: one set of bits, since the
+    blockwise kernel's summation order depends on K alone."""
+    p = synthetic.make_problem(M, K, L, seed=M + 3 * K + L)
+    ref, sums, sumabs = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    outs = []
+    for layout in (nv.SF_PLAIN, nv.SF_PERMUTED_128x4):
+        assert nv.nvfp4_gemv_plan(M, K, L, layout, sms, 0)["kernel"] == nv.KERNEL_BLOCKWISE
+        runs = [run(p, M, K, L, layout)]
+        if layout == nv.SF_PERMUTED_128x4:
+            runs.append(run(p, M, K, L, layout, via_gpu_repack=True))
+        for ctas in (1, 3, 40, 1000):
+            runs.append(run(p, M, K, L, layout, schedule=(nv.KERNEL_BLOCKWISE, 32, 1, ctas)))
+        for got in runs:
+            parity.assert_parity(got, ref, sums, sumabs, f"M={M} K={K} L={L} layout={layout}")
+        outs += runs
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+
+
+@pytest.mark.parametrize("M,K,L", [(150, 2560, 3), (128, 256, 1), (37, 16384, 1)])
+def test_blockwise_kernel_on_k_multiple_of_64(M, K, L):
+    p = synthetic.make_problem(M, K, L, seed=K + L)
+    ref, sums, sumabs = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
+    outs = []
+    for layout in (nv.SF_PLAIN, nv.SF_PERMUTED_128x4):
+        got = run(p, M, K, L, layout, schedule=(nv.KERNEL_BLOCKWISE, 32, 1, 64))
+        parity.assert_parity(got, ref, sums, sumabs, f"blockwise M={M} K={K} L={L}")
+        outs.append(got)
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_random_k16_shapes_default_schedule():
+    rng = np.random.default_rng(77)
+    for case in range(16):
+        M = int(rng.integers(1, 2000))
+        K = 16 * int(rng.integers(1, 400))
+        L = int(rng.integers(1, 5))
+        layout = int(rng.integers(0, 2))
+        p = synthetic.make_problem(M, K, L, seed=2000 + case)
+        ref, sums, sumabs = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
+        got = run(p, M, K, L, layout, via_gpu_repack=bool(case % 2))
+        parity.assert_parity(got, ref, sums, sumabs, f"case {case}: M={M} K={K} L={L} layout={layout}")
+
+
+def test_k16_large_sampled():
+    """A 59 MB A with K % 64 == 16, above nothing but the blockwise kernel's
+    own schedule: sampled outputs against the oracle."""
+    M, K, L = 7168, 16400, 1
+    p = synthetic.make_problem(M, K, L, seed=5)
+    mi, li = _sample_indices(M, L, 2000, np.random.default_rng(8))
+    ref, sums, sumabs = oracle.gemv_at(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L, mi, li)
+    for layout in (nv.SF_PLAIN, nv.SF_PERMUTED_128x4):
+        got = run(p, M, K, L, layout, via_gpu_repack=(layout == nv.SF_PERMUTED_128x4))
+        parity.assert_parity(got[li, mi], ref, sums, sumabs, f"M={M} K={K} layout={layout}")

@@ -43,6 +43,8 @@ def gpu_repack(src, rows, K, L, src_offset=0):
     (1000, 2048, 1), (4096, 64, 2), (7168, 2048, 4), (7168, 16384, 1), (333, 4160, 5),
     # K % 256 == 0 with 1, 3, 5 and 13 16-byte columns per plain row (partial column groups)
     (1, 256, 3), (129, 768, 3), (333, 1280, 2), (300, 3328, 3), (4096, 7168, 8),
+    # K % 64 != 0: the byte kernel, last atom column padded with 0x00
+    (1, 16, 1), (33, 48, 2), (130, 80, 3), (5, 1040, 1), (7168, 2064, 2), (300, 208, 1),
 ])
 @pytest.mark.parametrize("src_offset", [0, 4])
 def test_repack_bit_exact(rows, K, L, src_offset):
@@ -60,7 +62,8 @@ def test_repack_full_size_scales():
 
 
 def test_repack_overwrites_stale_padding():
-    for rows, K, L, off in [(5, 256, 2, 0), (5, 256, 2, 4), (5, 192, 2, 0)]:
+    for rows, K, L, off in [(5, 256, 2, 0), (5, 256, 2, 4), (5, 192, 2, 0), (5, 80, 2, 4),
+                            (130, 16, 1, 0)]:
         src = np.full((L, rows, K // 16), 0x38, dtype=np.uint8)
         got = gpu_repack(src, rows, K, L, off)  # dst pre-filled with 0xA5 by gpu_repack
         assert np.array_equal(got, oracle.repack_scales(src, rows, K, L))
