@@ -9,8 +9,10 @@ bracketed by CUDA events on the launching stream; that K-call window is
 repeated R times (until the windows add up to at least 0.5 s) and ``value``
 is the median over the windows of elapsed / K, in microseconds per call.
 Consecutive calls rotate over resident copies of the inputs (at least 2, and
-together more than 2x the 129 MB L2), so every call reads its operands from
-HBM (cold L2).  Consecutive calls do overlap: each call is launched with
+together at least 32x the 129 MB L2), so every call reads its operands from
+HBM (cold L2): the kernel streams A with an L2 evict_first policy, and such
+lines outlive a rotation of only 2x L2 (ncu: 25.5 of 33.1 MB per call read
+from DRAM there, 33.08 MB over 4 GB of sets).  Consecutive calls do overlap: each call is launched with
 programmatic stream serialization, so its CTAs start (and prefetch their first
 lines of A into L2) while the previous call's last CTAs finish.  Each line
 therefore also carries ``single_call_l2_flushed_us``: one event-bracketed call
@@ -37,7 +39,9 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -54,11 +58,18 @@ from nvfp4_block_scaled_gemv_gb300 import synthetic  # noqa: E402
 METRIC = "us/call (cold L2) and achieved HBM GB/s as % of GB300 peak, NVFP4 GEMV"
 UNIT = "us/call"
 WORKLOAD = synthetic.WORKLOADS[4]  # ("M16384_K8192_L16", 16384, 8192, 16)
-ROTATE_SETS = 8
+# Rotation for cold-L2 timing.  The GEMV streams A with an L2 evict_first
+# policy; measured with ncu on GB300 (dram__bytes_read.sum per call, graph of
+# back-to-back calls, no cache flush between them), M7168_K2048_L4 rotating
+# over 8 sets (265 MB, 2x L2) read 25.5 of its 33.1 MB per call from DRAM
+# (evict_first lines outlive the rotation), over 120 sets (4 GB) 33.08 MB.
+COLD_L2_MULTIPLE = 32
+MAX_SETS = 1024
 MIN_WINDOW_S = 0.5  # the timed K-call windows add up to at least this
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+KERNEL_NAMES = ("direct", "pipelined", "tensor", "blockdot", "blockwise")
 REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
 
@@ -77,7 +88,8 @@ def parse_args():
                          "small-N GEMM (lines after the headline)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--workload", default=WORKLOAD[0],
-                    choices=[w[0] for w in synthetic.WORKLOADS])
+                    help="one of " + ", ".join(w[0] for w in synthetic.WORKLOADS) +
+                         ", or any M<m>_K<k>_L<l>")
     ap.add_argument("--ncu", action="store_true",
                     help="only run warmup+steps calls of --workload (for profiler captures)")
     ap.add_argument("--schedule", default=None,
@@ -240,7 +252,7 @@ def profiled_traffic(workload: str, layout: str, schedule: dict):
 
 
 class DeviceProblem:
-    """ROTATE_SETS resident copies of one problem's inputs and outputs."""
+    """`sets` resident copies of one problem's inputs and outputs."""
 
     def __init__(self, torch, nv, p, M, K, L, layout, dev, sets):
         self.M, self.K, self.L, self.layout = M, K, L, layout
@@ -288,33 +300,48 @@ class ExtProblem(DeviceProblem):
                          b_batch_stride=self.b_stride, stream=stream_handle)
 
 
-def time_graph(torch, nv, prob, steps, warmup, stream, min_window_s=MIN_WINDOW_S):
+def time_graph(torch, nv, prob, steps, warmup, stream, min_window_s=MIN_WINDOW_S, period=None):
     """Microseconds per call over windows of `steps` back-to-back calls.
 
-    The calls are captured once into a CUDA graph (of g calls, g a divisor of
-    `steps`, replayed steps/g times per window).  Each window is bracketed by
-    its own pair of CUDA events on the launching stream; windows follow one
-    another until they add up to min_window_s.  Returns (median us per call
-    over the windows, (t0, t1) host monotonic bounds of the timed region,
-    calls timed, windows)."""
+    Call i uses input set i % period (period = len(prob.sets) by default).
+    The calls are captured into CUDA graphs of g calls each (g the largest
+    divisor of `steps` up to 64), graph j holding calls j*g .. j*g+g-1, as
+    many graphs as one full turn of the rotation takes; a window replays
+    steps/g of them in turn, continuing the rotation from the previous window.
+    Each window is bracketed by its own pair of CUDA events on the launching
+    stream; windows follow one another until they add up to min_window_s.
+    Returns (median us per call over the windows, (t0, t1) host monotonic
+    bounds of the timed region, calls timed, windows)."""
     handle = stream.cuda_stream
+    period = period or len(prob.sets)
     g_size = max(d for d in range(1, min(64, steps) + 1) if steps % d == 0)
+    n_graphs = period // math.gcd(period, g_size)
     with torch.cuda.stream(stream):
         for i in range(max(warmup, 3)):
             prob.call(nv, i, handle)
     stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(g_size):
-            prob.call(nv, i, handle)
-    # warm the graph and estimate one window's length
+    graphs = []
+    for j in range(n_graphs):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(j * g_size, (j + 1) * g_size):
+                prob.call(nv, i, handle)
+        graphs.append(graph)
+    turn = [0]
+
+    def replay_window():
+        for _ in range(steps // g_size):
+            graphs[turn[0]].replay()
+            turn[0] = (turn[0] + 1) % n_graphs
+
+    # warm every graph and estimate one window's length
     with torch.cuda.stream(stream):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        graph.replay()
-        e0.record(stream)
-        for _ in range(steps // g_size):
+        for graph in graphs:
             graph.replay()
+        e0.record(stream)
+        replay_window()
         e1.record(stream)
     stream.synchronize()
     est_s = max(e0.elapsed_time(e1) * 1e-3, 1e-6)
@@ -327,8 +354,7 @@ def time_graph(torch, nv, prob, steps, warmup, stream, min_window_s=MIN_WINDOW_S
     with torch.cuda.stream(stream):
         for s0, s1 in events:
             s0.record(stream)
-            for _ in range(steps // g_size):
-                graph.replay()
+            replay_window()
             s1.record(stream)
     stream.synchronize()
     t1 = time.monotonic()
@@ -449,7 +475,7 @@ def run_reference(args):
     rank, world, _ = rank_info()
     if rank != 0:
         return
-    name, M, K, L = next(w for w in synthetic.WORKLOADS if w[0] == args.workload)
+    name, M, K, L = workload_by_name(args.workload)
     p = synthetic.make_problem(M, K, L, seed=0)
     cores = host_cores()
     # every step is one bounded sample; the whole run stays within about a minute
@@ -476,15 +502,29 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def rotating_sets(nbytes: int) -> int:
-    """Input copies to rotate over: together more than 400 MB (> 2x L2), at least 2."""
-    return max(2, min(ROTATE_SETS, -(-400 * 2 ** 20 // nbytes)))
+def rotating_sets(nbytes: int, steps: int, l2: int) -> int:
+    """Input copies to rotate over: together at least COLD_L2_MULTIPLE x the L2
+    (at least 2, at most MAX_SETS), and a divisor of `steps` or a multiple of it
+    (so that a window of `steps` calls takes whole turns or whole fractions of
+    the rotation)."""
+    need = max(2, min(MAX_SETS, -(-COLD_L2_MULTIPLE * l2 // nbytes)))
+    if need <= steps:
+        return next(d for d in range(need, steps + 1) if steps % d == 0)
+    return -(-need // steps) * steps
+
+
+def l2_state(nbytes: int, sets: int, l2: int) -> str:
+    if sets * nbytes >= COLD_L2_MULTIPLE * l2:
+        return (f"{sets} rotating input sets, {sets * nbytes / 1e9:.2f} GB >= "
+                f"{COLD_L2_MULTIPLE}x L2 (cold L2 every call)")
+    return (f"{sets} rotating input sets, {sets * nbytes / 1e6:.1f} MB: less than "
+            f"{COLD_L2_MULTIPLE}x L2, inputs partly L2-resident")
 
 
 def kernel_name(nv, torch, dev, M, K, L, layout) -> str:
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     plan = nv.nvfp4_gemv_plan(M, K, L, layout, sms)
-    return ["direct", "pipelined", "tensor"][plan["kernel"]]
+    return KERNEL_NAMES[plan["kernel"]]
 
 
 def config_line(torch, nv, dev, stream, peaks, wname, wM, wK, wL, lay_name, steps, warmup):
@@ -493,9 +533,9 @@ def config_line(torch, nv, dev, stream, peaks, wname, wM, wK, wL, lay_name, step
     lay = nv.SF_PLAIN if lay_name == "plain" else nv.SF_PERMUTED_128x4
     wp = synthetic.make_problem(wM, wK, wL, seed=0)
     wbytes = synthetic.algorithmic_bytes(wM, wK, wL)
-    sets = rotating_sets(wbytes)
-    wprob = DeviceProblem(torch, nv, wp, wM, wK, wL, lay, dev, sets)
     wsteps = max(steps, 64)
+    sets = rotating_sets(wbytes, wsteps, l2_bytes(torch, dev))
+    wprob = DeviceProblem(torch, nv, wp, wM, wK, wL, lay, dev, sets)
     wus, _, calls, windows = time_graph(torch, nv, wprob, wsteps, max(warmup, 16), stream,
                                         min_window_s=0.25)
     smed, smin = time_single_flushed(torch, nv, wprob, 20, stream)
@@ -509,7 +549,8 @@ def config_line(torch, nv, dev, stream, peaks, wname, wM, wK, wL, lay_name, step
             "pct_of_hbm_peak": round(100 * gbs / peaks["hbm_gbs"], 2),
             "single_call_l2_flushed_us": round(smed, 3),
             "single_call_pct_of_hbm_peak": round(100 * sgbs / peaks["hbm_gbs"], 2),
-            "rotating_sets": sets, "calls": calls, "windows": windows}
+            "rotating_sets": sets, "l2": l2_state(wbytes, sets, l2_bytes(torch, dev)),
+            "calls": calls, "windows": windows}
 
 
 def run_native(args):
@@ -530,7 +571,7 @@ def run_native(args):
     stream = torch.cuda.Stream(device=dev)
     peaks = measured_peaks()
 
-    name, M, K, L = next(w for w in synthetic.WORKLOADS if w[0] == args.workload)
+    name, M, K, L = workload_by_name(args.workload)
     layout = nv.SF_PLAIN if args.layout == "plain" else nv.SF_PERMUTED_128x4
 
     # the other workloads and layouts first (the headline line is printed last)
@@ -548,7 +589,8 @@ def run_native(args):
 
     p = synthetic.make_problem(M, K, L, seed=0)
     nbytes = synthetic.algorithmic_bytes(M, K, L)
-    sets = rotating_sets(nbytes)
+    l2 = l2_bytes(torch, dev)
+    sets = rotating_sets(nbytes, args.steps, l2)
     prob = DeviceProblem(torch, nv, p, M, K, L, layout, dev, sets)
 
     sampler = ClockSampler(gpu_id_for_smi(torch, local)) if rank == 0 else None
@@ -580,14 +622,13 @@ def run_native(args):
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "e2m1xe4m3->f32->f16", "data": "synthetic",
         "config": {"workload": name, "M": M, "K": K, "L": L, "scale_layout": args.layout,
-                   "l2": f"{sets} rotating input sets, {sets * nbytes / 1e6:.0f} MB "
-                         "> 2x L2 (cold L2 every call)",
+                   "l2": l2_state(nbytes, sets, l2),
                    "launch": "CUDA graph of back-to-back nvfp4_gemv calls with programmatic "
                              "stream serialization: each call's CTAs start, and prefetch their "
                              "first A lines into L2, while the previous call's last CTAs finish",
                    "timing": f"{windows} event-bracketed windows of {args.steps} calls, median",
                    "bytes_per_call": nbytes, "schedule": plan,
-                   "kernel": ["direct", "pipelined", "tensor"][plan["kernel"]]},
+                   "kernel": KERNEL_NAMES[plan["kernel"]]},
         "gb_per_s": round(achieved, 1),
         "pct_of_hbm_peak": round(100 * achieved / peaks["hbm_gbs"], 2),
         "single_call_l2_flushed_us": {"median": round(single_med, 3), "min": round(single_min, 3),
@@ -616,7 +657,8 @@ def run_native(args):
             src0 = torch.from_numpy(wp["sfa"]).to(dev)
             out_bytes = nv.nvfp4_permuted_scale_bytes(wM, wK, wL)
             rbytes = src0.numel() + out_bytes
-            sets = max(2, min(ROTATE_SETS, -(-400 * 2 ** 20 // rbytes)))
+            rsteps = 64
+            sets = rotating_sets(rbytes, rsteps, l2)
             srcs = [src0.clone() for _ in range(sets)]
             dsts = [torch.empty(out_bytes, dtype=torch.uint8, device=dev) for _ in range(sets)]
             del src0
@@ -626,8 +668,7 @@ def run_native(args):
                     nv_.nvfp4_repack_scales(srcs[i % sets].data_ptr(), dsts[i % sets].data_ptr(),
                                             wM, wK, wL, h)
 
-            rsteps = 64
-            rus, _, _, _ = time_graph(torch, nv, _Repack(), rsteps, 64, stream, 0.25)
+            rus, _, _, _ = time_graph(torch, nv, _Repack(), rsteps, 64, stream, 0.25, period=sets)
             gbs = rbytes / (rus * 1e-6) / 1e9
             print(json.dumps({"workload": wname, "kernel": "repack_scales (sfa)",
                               "us_per_call": round(rus, 3), "bytes_per_call": rbytes,
@@ -640,15 +681,16 @@ def run_native(args):
         wname, wM, wK, wL = synthetic.WORKLOADS[1]
         wp = synthetic.make_problem(wM, wK, wL, seed=0)
         wbytes = synthetic.algorithmic_bytes(wM, wK, wL) + 2 * wL * wM  # + the bias
-        wprob = ExtProblem(torch, nv, wp, wM, wK, wL, nv.SF_PLAIN, dev, ROTATE_SETS)
         wsteps = 64
+        wsets = rotating_sets(wbytes, wsteps, l2)
+        wprob = ExtProblem(torch, nv, wp, wM, wK, wL, nv.SF_PLAIN, dev, wsets)
         wus, _, _, _ = time_graph(torch, nv, wprob, wsteps, 64, stream, 0.25)
         gbs = wbytes / (wus * 1e-6) / 1e9
         print(json.dumps({"workload": wname, "scale_layout": "plain",
                           "path": "nvfp4_gemv_ex: alpha 0.5, fp16 bias, b in an [L][8][K/2] buffer",
                           "us_per_call": round(wus, 3), "gb_per_s": round(gbs, 1),
                           "pct_of_hbm_peak": round(100 * gbs / peaks["hbm_gbs"], 2),
-                          "rotating_sets": ROTATE_SETS, "calls": wsteps}), flush=True)
+                          "rotating_sets": wsets, "calls": wsteps}), flush=True)
         del wprob
         torch.cuda.empty_cache()
         # the small-N GEMM (tensor-core kernel) on the decode-batch workloads;
@@ -656,7 +698,8 @@ def run_native(args):
         for gname, gM, gN, gK, gL in synthetic.GEMM_WORKLOADS:
             gp = synthetic.make_gemm_problem(gM, gN, gK, gL, seed=0)
             gbytes = synthetic.gemm_algorithmic_bytes(gM, gN, gK, gL)
-            gsets = max(2, min(ROTATE_SETS, -(-400 * 2 ** 20 // gbytes)))
+            gsteps = 64
+            gsets = rotating_sets(gbytes, gsteps, l2)
             a0 = torch.from_numpy(gp["a"]).to(dev)
             b0 = torch.from_numpy(gp["b"]).to(dev)
             sa0 = nv.repack_scales(torch.from_numpy(gp["sfa"]).to(dev))
@@ -672,8 +715,7 @@ def run_native(args):
                                            x[3].data_ptr(), x[4].data_ptr(), gM, gN, gK, gL,
                                            stream=h)
 
-            gsteps = 64
-            gus, _, _, _ = time_graph(torch, nv, _Gemm(), gsteps, 64, stream, 0.25)
+            gus, _, _, _ = time_graph(torch, nv, _Gemm(), gsteps, 64, stream, 0.25, period=gsets)
             gbs = gbytes / (gus * 1e-6) / 1e9
             print(json.dumps({"workload": gname, "path": "nvfp4_gemm_small_n (tensor cores)",
                               "N": gN, "us_per_call": round(gus, 3), "bytes_per_call": gbytes,
@@ -683,6 +725,17 @@ def run_native(args):
             del gs
             torch.cuda.empty_cache()
         assert nv.nvfp4_tensor_wait_timeouts(reset=True) == 0, "a tensor-core pipeline wait ran out"
+
+
+def workload_by_name(name: str):
+    """(name, M, K, L) of a benchmark workload, or of any "M<m>_K<k>_L<l>"."""
+    for w in synthetic.WORKLOADS:
+        if w[0] == name:
+            return w
+    m = re.fullmatch(r"M(\d+)_K(\d+)_L(\d+)", name)
+    if not m:
+        raise SystemExit(f"unknown workload {name!r}")
+    return (name, int(m.group(1)), int(m.group(2)), int(m.group(3)))
 
 
 def run_profile_case(args):
@@ -712,7 +765,7 @@ def run_profile_case(args):
         assert nv.nvfp4_tensor_wait_timeouts(reset=True) == 0
         print(f"profile case done: {gname} small-N GEMM {args.warmup}+{args.steps} calls")
         return
-    name, M, K, L = next(w for w in synthetic.WORKLOADS if w[0] == args.workload)
+    name, M, K, L = workload_by_name(args.workload)
     layout = nv.SF_PLAIN if args.layout == "plain" else nv.SF_PERMUTED_128x4
     p = synthetic.make_problem(M, K, L, seed=0)
     stream = torch.cuda.Stream(device=dev)

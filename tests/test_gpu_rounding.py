@@ -49,12 +49,12 @@ def _runs(M, K, L, layout):
     the shape and layout: the library's own choice, then each kernel's plan."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     out = [("default", None)]
-    kernels = [nv.KERNEL_PIPELINED, nv.KERNEL_BLOCKDOT]
+    kernels = [nv.KERNEL_PIPELINED, nv.KERNEL_BLOCKDOT, nv.KERNEL_BLOCKWISE]
     if layout == nv.SF_PERMUTED_128x4:
         kernels.append(nv.KERNEL_TENSOR)
     for k in kernels:
         plan = nv.nvfp4_gemv_plan(M, K, L, layout, sms, 0, kernel=k)
-        out.append((["direct", "pipelined", "tensor", "blockdot"][k],
+        out.append((["direct", "pipelined", "tensor", "blockdot", "blockwise"][k],
                     (k, plan["lanes_per_row"], plan["k_split"], plan["ctas"])))
     return out
 
