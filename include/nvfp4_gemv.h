@@ -107,8 +107,30 @@ nvfp4_status_t nvfp4_gemv(const void* a, const void* b, const void* sfa, const v
                           struct CUstream_st* stream);
 
 /*
+ * Output activation of nvfp4_gemv_ex and nvfp4_gemm_small_n, applied in fp32
+ * to y = alpha * sum + bias before the fp16 rounding: c = fp16(act(y)).  The
+ * pages list none; these are the usual MLP activations, with NaN in -> NaN out:
+ *   NVFP4_ACT_NONE      act(y) = y
+ *   NVFP4_ACT_RELU      act(y) = y > 0 ? y : +0
+ *   NVFP4_ACT_SILU      act(y) = y / (1 + exp(-y))
+ *   NVFP4_ACT_GELU_TANH act(y) = y/2 * (1 + tanh(sqrt(2/pi) * (y + 0.044715 y^3)))
+ *   NVFP4_ACT_GELU_ERF  act(y) = y/2 * (1 + erf(y / sqrt(2)))
+ * Accuracy: act is evaluated with CUDA's fp32 expf, tanhf and erff; |act'| <=
+ * 1.13 for all five, so c stays within 1.13 * (1e-3 * |alpha| * sum|terms|) + 1
+ * fp16 ulp of act applied to the exact value (plus the fp32 evaluation error,
+ * a few fp32 ulps).
+ */
+typedef enum {
+  NVFP4_ACT_NONE = 0,
+  NVFP4_ACT_RELU = 1,
+  NVFP4_ACT_SILU = 2,
+  NVFP4_ACT_GELU_TANH = 3,
+  NVFP4_ACT_GELU_ERF = 4
+} nvfp4_activation_t;
+
+/*
  * Options of nvfp4_gemv_ex.  Zero-initialised fields other than alpha give
- * the plain call; {1.0f, NULL, 0, 0} is exactly nvfp4_gemv.
+ * the plain call; {1.0f, NULL, 0, 0, NVFP4_ACT_NONE} is exactly nvfp4_gemv.
  *
  *   alpha            : fp32 output scale: c = fp16(alpha * sum + bias).  A
  *                      global per-tensor scale of this kind is mentioned in a
@@ -125,14 +147,17 @@ nvfp4_status_t nvfp4_gemv(const void* a, const void* b, const void* sfa, const v
  *   sfb_batch_stride : bytes from batch l to batch l+1 of sfb; 0 = dense
  *                      (K/16 plain, ceil(K/64)*512 permuted).  Otherwise at least
  *                      that, and a multiple of 4 (plain) or 16 (permuted).
- * Violations: a stride below the dense size -> NVFP4_ERR_INVALID_VALUE; a
- * stride or bias pointer off its alignment -> NVFP4_ERR_MISALIGNED.
+ *   activation       : nvfp4_activation_t, applied last (see above).
+ * Violations: a stride below the dense size or an unknown activation ->
+ * NVFP4_ERR_INVALID_VALUE; a stride or bias pointer off its alignment ->
+ * NVFP4_ERR_MISALIGNED.
  */
 typedef struct {
   float alpha;
   const void* bias;
   int64_t b_batch_stride;
   int64_t sfb_batch_stride;
+  int32_t activation;
 } nvfp4_gemv_options_t;
 
 /*

@@ -61,6 +61,7 @@ KERNEL_PIPELINED = 1
 KERNEL_TENSOR = 2
 KERNEL_BLOCKDOT = 3
 KERNEL_BLOCKWISE = 4
+ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU_TANH, ACT_GELU_ERF = 0, 1, 2, 3, 4
 
 
 class _Plan(ctypes.Structure):
@@ -71,7 +72,8 @@ class _Plan(ctypes.Structure):
 
 class _Options(ctypes.Structure):
     _fields_ = [("alpha", ctypes.c_float), ("bias", ctypes.c_void_p),
-                ("b_batch_stride", ctypes.c_int64), ("sfb_batch_stride", ctypes.c_int64)]
+                ("b_batch_stride", ctypes.c_int64), ("sfb_batch_stride", ctypes.c_int64),
+                ("activation", ctypes.c_int32)]
 
 
 _lib = None
@@ -135,10 +137,11 @@ def nvfp4_gemv(a: int, b: int, sfa: int, sfb: int, c: int, M: int, K: int, L: in
 
 def nvfp4_gemv_ex(a: int, b: int, sfa: int, sfb: int, c: int, M: int, K: int, L: int,
                   sf_layout: int = SF_PLAIN, alpha: float = 1.0, bias: int = 0,
-                  b_batch_stride: int = 0, sfb_batch_stride: int = 0, stream: int = 0) -> None:
-    """nvfp4_gemv with an output scale, an fp16 [L][M] bias (pointer or 0) and
-    batch strides for b and sfb (0 = dense)."""
-    opt = _Options(alpha, bias or None, b_batch_stride, sfb_batch_stride)
+                  b_batch_stride: int = 0, sfb_batch_stride: int = 0, stream: int = 0,
+                  activation: int = 0) -> None:
+    """nvfp4_gemv with an output scale, an fp16 [L][M] bias (pointer or 0),
+    batch strides for b and sfb (0 = dense) and an output activation (ACT_*)."""
+    opt = _Options(alpha, bias or None, b_batch_stride, sfb_batch_stride, activation)
     _check(library().nvfp4_gemv_ex(a, b, sfa, sfb, c, M, K, L, sf_layout, ctypes.byref(opt),
                                    stream), "nvfp4_gemv_ex")
 
@@ -154,10 +157,10 @@ def nvfp4_gemv_explicit(a: int, b: int, sfa: int, sfb: int, c: int, M: int, K: i
 
 def nvfp4_gemm_small_n(a: int, b: int, sfa: int, sfb: int, c: int, M: int, N: int, K: int,
                        L: int, alpha: float = 1.0, bias: int = 0, b_batch_stride: int = 0,
-                       sfb_batch_stride: int = 0, stream: int = 0) -> None:
+                       sfb_batch_stride: int = 0, stream: int = 0, activation: int = 0) -> None:
     """Small-N GEMM: c [L][N][M] from a [L][M][K/2], b [L][N][K/2] and
     pre-permuted scales (sfb: the permuted form of [L][N][K/16])."""
-    opt = _Options(alpha, bias or None, b_batch_stride, sfb_batch_stride)
+    opt = _Options(alpha, bias or None, b_batch_stride, sfb_batch_stride, activation)
     _check(library().nvfp4_gemm_small_n(a, b, sfa, sfb, c, M, N, K, L, ctypes.byref(opt),
                                         stream), "nvfp4_gemm_small_n")
 

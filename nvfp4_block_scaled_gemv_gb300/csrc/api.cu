@@ -1,6 +1,7 @@
 // C ABI: argument validation, launch planning and dispatch.
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cstdint>
 
 #include "internal.h"
@@ -88,11 +89,14 @@ nvfp4_status_t validate_gemv_pointers(const void* a, const void* b, const void* 
 
 // The options of a plain nvfp4_gemv call: no output scale or bias, dense b
 // and sfb (strides 0 = dense).
-const nvfp4_gemv_options_t kDefaultOptions = {1.0f, nullptr, 0, 0};
+const nvfp4_gemv_options_t kDefaultOptions = {1.0f, nullptr, 0, 0, NVFP4_ACT_NONE};
+
+bool activation_ok(int32_t act) { return act >= NVFP4_ACT_NONE && act <= NVFP4_ACT_GELU_ERF; }
 
 // Option checks shared by the entry points that take options.
 nvfp4_status_t validate_options(const nvfp4_gemv_options_t& o, int64_t K, int sf_layout) {
   if (o.b_batch_stride < 0 || o.sfb_batch_stride < 0) return NVFP4_ERR_INVALID_VALUE;
+  if (!activation_ok(o.activation)) return NVFP4_ERR_INVALID_VALUE;
   if (o.b_batch_stride != 0 && o.b_batch_stride < K / 2) return NVFP4_ERR_INVALID_VALUE;
   if (o.b_batch_stride % 16 != 0) return NVFP4_ERR_MISALIGNED;
   const bool permuted = sf_layout == NVFP4_SF_PERMUTED_128x4;
@@ -139,6 +143,7 @@ GemvParams make_params(const void* a, const void* b, const void* sfa, const void
                                            : (permuted ? (int64_t)p.rest_k * 512 : K / 16);
   p.alpha = opt.alpha;
   p.bias = static_cast<const uint16_t*>(opt.bias);
+  p.activation = opt.activation;
   return p;
 }
 
@@ -257,6 +262,7 @@ nvfp4_status_t validate_gemm(const void* a, const void* b, const void* sfa, cons
   if (M != 0 && L > kMaxRows / M) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (L * ((M + 127) / 128) > 0x7fffffff) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (o.b_batch_stride < 0 || o.sfb_batch_stride < 0) return NVFP4_ERR_INVALID_VALUE;
+  if (!activation_ok(o.activation)) return NVFP4_ERR_INVALID_VALUE;
   if (o.b_batch_stride != 0 && o.b_batch_stride < N * (K / 2)) return NVFP4_ERR_INVALID_VALUE;
   if (o.sfb_batch_stride != 0 && o.sfb_batch_stride < (K / 64) * 512) return NVFP4_ERR_INVALID_VALUE;
   if (o.b_batch_stride % 16 != 0 || o.sfb_batch_stride % 16 != 0) return NVFP4_ERR_MISALIGNED;
@@ -390,7 +396,9 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
     return true;
   }
   if (K % 64 != 0) return false;
-  const int64_t a_bytes = M * L * (K / 2);
+  // bytes of A, saturated (M*L < 2^40 and K/2 <= 2^29 can pass 2^63)
+  const int64_t a_bytes =
+      K / 2 > 0 && M * L > INT64_MAX / (K / 2) ? INT64_MAX : M * L * (K / 2);
   // Tiny problems with plain scales (measured on GB300 over 16 KB .. 2 MB of
   // A): the launch and the first DRAM access dominate, and fewer, fuller CTAs
   // finish first.  Up to 512 KB the direct kernel does best with rows narrow
@@ -706,6 +714,7 @@ nvfp4_status_t nvfp4_gemm_small_n_plan(int64_t M, int64_t N, int64_t K, int64_t 
                                     kDefaultOptions);
   if (st != NVFP4_OK) return st;
   if (M < 0 || M > kMaxM || (M != 0 && L > kMaxRows / M)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (L * ((M + 127) / 128) > 0x7fffffff) return NVFP4_ERR_UNSUPPORTED_SHAPE;  // 128-row tiles
   cudaError_t err = plan_tc(M, N < 1 ? 1 : N, K, L, stages, k_split, ctas);
   if (err == cudaSuccess && resident_ctas != nullptr)
     err = tc_resident_clusters(2, N < 1 ? 1 : N, 1, resident_ctas);

@@ -70,6 +70,7 @@
 
 #include <cuda_fp16.h>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
 
@@ -105,6 +106,7 @@ struct BdParams {
   uint16_t* c;           // fp16 [L][M]
   const uint16_t* bias;  // fp16 [L][M], or null
   float alpha;
+  int32_t activation;    // nvfp4_activation_t
   int64_t M;
   int64_t sfb_stride;
   int64_t units_per_l;   // 8-row units per batch
@@ -162,11 +164,9 @@ struct BdTiles {
   }
 };
 
-// fp32 -> fp16 output with the optional scale and bias (the CUDA-core
-// kernels' epilogue formula).
+// fp32 -> fp16 output (the epilogue of every kernel).
 __device__ __forceinline__ uint16_t bd_finish(const BdParams& p, float v, int64_t idx) {
-  const float o = p.bias ? fmaf(v, p.alpha, __half2float(__ushort_as_half(p.bias[idx]))) : v * p.alpha;
-  return __half_as_ushort(__float2half_rn(o));
+  return finish_value(v, p.alpha, p.bias, p.activation, idx);
 }
 
 // sfa * sfb of one block, exact in fp32: the low (HI = false) or high halves
@@ -564,6 +564,7 @@ cudaError_t launch_blockdot(const GemvParams& gp, bool permuted, int64_t L, int 
   p.c = gp.c;
   p.bias = gp.bias;
   p.alpha = gp.alpha;
+  p.activation = gp.activation;
   p.M = gp.M;
   p.sfb_stride = gp.sfb_stride;
   p.units_per_l = (gp.M + ur - 1) / ur;

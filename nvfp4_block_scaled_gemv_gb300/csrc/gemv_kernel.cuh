@@ -29,6 +29,7 @@
 #pragma once
 #include <cuda_fp16.h>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -77,9 +78,7 @@ __device__ __forceinline__ int batch_of(const GemvParams& p, int64_t r) {
 // nearest even, with one fp32 rounding before it (a fused multiply-add when
 // there is a bias; alpha = 1 without one gives v itself).
 __device__ __forceinline__ uint16_t finish_output(const GemvParams& p, float v, int64_t idx) {
-  const float o = p.bias ? fmaf(v, p.alpha, __half2float(__ushort_as_half(p.bias[idx])))
-                         : v * p.alpha;
-  return __half_as_ushort(__float2half_rn(o));
+  return finish_value(v, p.alpha, p.bias, p.activation, idx);
 }
 
 // Byte offset of the 4 scale bytes (blocks 4kt..4kt+3) of row m, chunk 0.

@@ -47,11 +47,13 @@
 // timeout in a device word the host can read, and the thread then skips its
 // remaining work; control flow stays uniform so every thread reaches the
 // cluster barriers and TMEM is always freed.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
 #include <cuda_fp16.h>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
 
@@ -97,15 +99,9 @@ struct TcParams {
   int64_t M;
   int64_t sfb_stride;  // bytes from batch l to l+1 of sfb
   int32_t N, rest_m, rest_k, kstages, tiles;
+  int32_t activation;  // nvfp4_activation_t
 };
 
-// fp32 -> fp16 output with the optional scale and bias: the same formula as
-// the CUDA-core kernels' epilogue.
-__device__ __forceinline__ uint16_t finish_output_tc(float alpha, const uint16_t* bias, float v,
-                                                     int64_t idx) {
-  const float o = bias ? fmaf(v, alpha, __half2float(__ushort_as_half(bias[idx]))) : v * alpha;
-  return __half_as_ushort(__float2half_rn(o));
-}
 
 // The MMA reads each scale byte as an unsigned E4M3 magnitude (the sign bit
 // is ignored).  A negative scale is folded into the operand it scales: for
@@ -398,7 +394,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int n = 0; n < NC; ++n) {
           if (n < p.N) {
             const int64_t idx = ((int64_t)l * p.N + n) * p.M + m;
-            p.c[idx] = finish_output_tc(p.alpha, p.bias, part[n], idx);
+            p.c[idx] = finish_value(part[n], p.alpha, p.bias, p.activation, idx);
           }
         }
       }
@@ -474,6 +470,41 @@ cudaError_t tc_launch_config(TcKernel kern, int stages, int nc, cudaLaunchConfig
   return cudaSuccess;
 }
 
+// The static_asserts above, on the current device: shared memory must keep
+// the CTAs resident on one SM within its 512 TMEM columns (at most 4 CTAs of
+// 2 stages, 2 of 4 stages, 2 of 2 stages beside one of 4), so that no
+// tcgen05.alloc ever waits for another CTA.  The smallest footprints (one
+// column of B) are the ones that pack most CTAs.  Checked once per device.
+cudaError_t tc_tmem_never_oversubscribed(bool* ok) {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cached[kMaxDevices];  // 0 unknown, 1 ok, 2 not
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c != 0) {
+      *ok = c == 1;
+      return cudaSuccess;
+    }
+  }
+  int smem_sm = 0, reserved = 0;
+  if ((err = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+          cudaSuccess ||
+      (err = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+          cudaSuccess)
+    return err;
+  int64_t cta[2];
+  for (int i = 0; i < 2; ++i) {
+    cudaFuncAttributes fa;
+    if ((err = cudaFuncGetAttributes(&fa, tc_kernel_for(2 + 2 * i, 1))) != cudaSuccess) return err;
+    cta[i] = (int64_t)tc_smem_bytes(2 + 2 * i, 1) + (int64_t)fa.sharedSizeBytes + reserved;
+  }
+  *ok = 5 * cta[0] > smem_sm && 3 * cta[1] > smem_sm && cta[1] + 3 * cta[0] > smem_sm;
+  if (dev >= 0 && dev < kMaxDevices) cached[dev].store(*ok ? 1 : 2, std::memory_order_relaxed);
+  return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_gemv_tc(const GemvParams& gp, int64_t N, int64_t L, int64_t b_row_stride,
@@ -481,6 +512,10 @@ cudaError_t launch_gemv_tc(const GemvParams& gp, int64_t N, int64_t L, int64_t b
   const int nc = tc_columns(N);
   TcKernel kern = tc_kernel_for(stages, nc);
   if (kern == nullptr || N < 1 || N > 16) return cudaErrorInvalidValue;
+  bool tmem_ok = false;
+  cudaError_t terr = tc_tmem_never_oversubscribed(&tmem_ok);
+  if (terr != cudaSuccess) return terr;
+  if (!tmem_ok) return cudaErrorNotSupported;
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (encode == nullptr && gp.half_k > 0) return cudaErrorNotSupported;
   TcParams p;
@@ -511,6 +546,7 @@ cudaError_t launch_gemv_tc(const GemvParams& gp, int64_t N, int64_t L, int64_t b
   p.c = gp.c;
   p.bias = gp.bias;
   p.alpha = gp.alpha;
+  p.activation = gp.activation;
   p.M = gp.M;
   p.sfb_stride = gp.sfb_stride;
   p.N = (int32_t)N;

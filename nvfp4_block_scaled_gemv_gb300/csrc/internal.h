@@ -50,6 +50,7 @@ struct GemvParams {
   int32_t steps;      // ceil(kchunks / lanes_per_row)
   int32_t rest_m;     // ceil(M/128)
   int32_t rest_k;     // ceil(K/64): atom columns of a pre-permuted row
+  int32_t activation; // nvfp4_activation_t applied to the output
 };
 
 struct GemvPlan {

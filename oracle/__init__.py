@@ -19,6 +19,7 @@ fp16 bit patterns [L, M] (uint16).
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 
@@ -133,24 +134,60 @@ def gemv(a, b, sfa, sfb, M: int, K: int, L: int):
     return c, s, sabs
 
 
-def gemv_ex(a, b, sfa, sfb, M: int, K: int, L: int, alpha: float = 1.0, bias=None):
-    """fp64 path with an output scale and bias: ``fp16(alpha * sum + bias)``.
+# Output activations (codes of the library's nvfp4_activation_t), their
+# textbook definitions, and a bound on |act'| over the reals: an error e in
+# the activation's input moves its output by at most LIPSCHITZ * e.
+ACT_NONE, ACT_RELU, ACT_SILU, ACT_GELU_TANH, ACT_GELU_ERF = 0, 1, 2, 3, 4
+LIPSCHITZ = {ACT_NONE: 1.0, ACT_RELU: 1.0, ACT_SILU: 1.1, ACT_GELU_TANH: 1.13,
+             ACT_GELU_ERF: 1.13}
 
-    ``bias`` is fp16 bits [L, M] (uint16) or None.  ``alpha * sum + bias`` is
-    formed in fp64 from the fp64 sums of :func:`gemv` and rounded to binary16
-    once.  Returns ``(c_bits, values, |alpha| * sumabs)``: the fp64 values
-    before rounding and the |term| sums scaled like the sums (the tolerance).
+
+def activate(y, act: int) -> np.ndarray:
+    """act(y) in fp64, NaN in -> NaN out:
+
+    * ReLU: y if y > 0 else +0;
+    * SiLU (sigmoid-weighted linear unit): y * sigmoid(y) = y / (1 + exp(-y));
+    * GELU, tanh form: y/2 * (1 + tanh(sqrt(2/pi) * (y + 0.044715 * y^3)));
+    * GELU, erf form: y/2 * (1 + erf(y / sqrt(2))) = y * Phi(y).
+    """
+    y = np.asarray(y, dtype=np.float64)
+    if act == ACT_NONE:
+        return y
+    if act == ACT_RELU:
+        return np.where(y > 0, y, np.where(np.isnan(y), y, 0.0))
+    with np.errstate(over="ignore", invalid="ignore"):
+        if act == ACT_SILU:
+            return y / (1.0 + np.exp(-y))
+        if act == ACT_GELU_TANH:
+            return 0.5 * y * (1.0 + np.tanh(math.sqrt(2.0 / math.pi) * (y + 0.044715 * y ** 3)))
+        if act == ACT_GELU_ERF:
+            erf = np.vectorize(math.erf, otypes=[np.float64])
+            return 0.5 * y * (1.0 + erf(y / math.sqrt(2.0)))
+    raise ValueError(f"unknown activation {act}")
+
+
+def gemv_ex(a, b, sfa, sfb, M: int, K: int, L: int, alpha: float = 1.0, bias=None,
+            activation: int = ACT_NONE):
+    """fp64 path with an output scale, bias and activation:
+    ``fp16(act(alpha * sum + bias))``.
+
+    ``bias`` is fp16 bits [L, M] (uint16) or None.  ``act(alpha * sum + bias)``
+    is formed in fp64 from the fp64 sums of :func:`gemv` and rounded to
+    binary16 once.  Returns ``(c_bits, values, LIPSCHITZ[act] * |alpha| *
+    sumabs)``: the fp64 values before rounding and the |term| sums scaled like
+    the sums (the tolerance).
     """
     _, s, sabs = gemv(a, b, sfa, sfb, M, K, L)
     y = np.float64(alpha) * s
     if bias is not None:
         bv = np.ascontiguousarray(np.asarray(bias, dtype=np.uint16)).view(np.float16)
         y = y + bv.astype(np.float64).reshape(L, M)
-    return fp16_rne(y), y, abs(float(alpha)) * sabs
+    y = activate(y, activation)
+    return fp16_rne(y), y, LIPSCHITZ[activation] * abs(float(alpha)) * sabs
 
 
 def gemm_small_n(a, b, sfa, sfb, M: int, N: int, K: int, L: int, alpha: float = 1.0,
-                 bias=None):
+                 bias=None, activation: int = ACT_NONE):
     """Small-N GEMM: N dot products per row of A, one per vector of b::
 
         c[l, n, m] = fp16(alpha * sum_k E2M1(a[m,k,l]) * E4M3(sfa[m,k//16,l])
@@ -172,7 +209,7 @@ def gemm_small_n(a, b, sfa, sfb, M: int, N: int, K: int, L: int, alpha: float = 
         bn = None if bias_ is None else np.ascontiguousarray(bias_[:, n, :])
         c[:, n, :], vals[:, n, :], tol[:, n, :] = gemv_ex(
             a, np.ascontiguousarray(b_[:, n, :]), sfa, np.ascontiguousarray(sb_[:, n, :]),
-            M, K, L, alpha, bn)
+            M, K, L, alpha, bn, activation)
     return c, vals, tol
 
 

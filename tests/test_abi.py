@@ -528,3 +528,40 @@ def test_gemm_small_n_plan_validation(lib):
     assert lib.nvfp4_gemm_small_n_plan(-1, 4, 1024, 2, *args) == nv.ERR_UNSUPPORTED_SHAPE
     assert lib.nvfp4_gemm_small_n_plan(300, 4, 1024, 2, None, None, None, None) == \
         nv.ERR_INVALID_VALUE
+
+
+def test_options_validation(lib):
+    """nvfp4_gemv_ex / nvfp4_gemm_small_n options, checked before any CUDA call."""
+    import ctypes
+
+    def opt(**kw):
+        o = nv._Options(1.0, None, 0, 0, 0)
+        for k, v in kw.items():
+            setattr(o, k, v)
+        return ctypes.byref(o)
+
+    args = (64, 64, 64, 64, 64, 8, 256, 2, 0)
+    for act in (-1, 5, 99):
+        assert lib.nvfp4_gemv_ex(*args, opt(activation=act), None) == nv.ERR_INVALID_VALUE
+        assert lib.nvfp4_gemm_small_n(64, 64, 64, 64, 64, 8, 4, 256, 2, opt(activation=act),
+                                      None) == nv.ERR_INVALID_VALUE
+    assert lib.nvfp4_gemv_ex(*args, opt(b_batch_stride=-16), None) == nv.ERR_INVALID_VALUE
+    assert lib.nvfp4_gemv_ex(*args, opt(b_batch_stride=64), None) == nv.ERR_INVALID_VALUE  # < K/2
+    assert lib.nvfp4_gemv_ex(*args, opt(b_batch_stride=136), None) == nv.ERR_MISALIGNED
+    assert lib.nvfp4_gemv_ex(*args, opt(bias=65), None) == nv.ERR_MISALIGNED
+    # empty problems with a valid activation are no-ops
+    for act in range(5):
+        assert lib.nvfp4_gemv_ex(None, None, None, None, None, 0, 256, 2, 0, opt(activation=act),
+                                 None) == nv.OK
+
+
+def test_huge_shapes_plan_without_overflow(lib):
+    # M*L*K/2 beyond 2^63: the byte count saturates instead of wrapping into
+    # the tiny-problem schedule
+    M, K, L = (1 << 31) - 1, 1 << 30, 500
+    plan = nv.nvfp4_gemv_plan(M, K, L, nv.SF_PLAIN, 152, 2)
+    assert plan["kernel"] == nv.KERNEL_PIPELINED and plan["ctas"] == 304
+    # the small-N GEMM's 128-row tiles must number below 2^31
+    st, ks, ctas = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
+    assert lib.nvfp4_gemm_small_n_plan(M, 4, 1024, 200, ctypes.byref(st), ctypes.byref(ks),
+                                       ctypes.byref(ctas), None) == nv.ERR_UNSUPPORTED_SHAPE

@@ -37,7 +37,7 @@ def to_dev(x):
     return torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
 
 
-def run_gemm(p, M, N, K, L, schedule=None, alpha=1.0, bias=None, b_pad_rows=0):
+def run_gemm(p, M, N, K, L, schedule=None, alpha=1.0, bias=None, b_pad_rows=0, activation=0):
     """c bits [L, N, M]; schedule = (stages, k_split, ctas) for the explicit call.
     b_pad_rows > 0 puts b in an [L][N + b_pad_rows][K/2] buffer (batch stride)."""
     a = to_dev(p["a"])
@@ -64,9 +64,9 @@ def run_gemm(p, M, N, K, L, schedule=None, alpha=1.0, bias=None, b_pad_rows=0):
         nv.nvfp4_gemm_small_n(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(),
                               c.data_ptr(), M, N, K, L, alpha=alpha,
                               bias=bias_t.data_ptr() if bias_t is not None else 0,
-                              b_batch_stride=b_stride, stream=stream)
+                              b_batch_stride=b_stride, stream=stream, activation=activation)
     else:
-        assert alpha == 1.0 and bias is None and not b_pad_rows
+        assert alpha == 1.0 and bias is None and not b_pad_rows and not activation
         nv.nvfp4_gemm_small_n_explicit(a.data_ptr(), b.data_ptr(), sfa.data_ptr(),
                                        sfb.data_ptr(), c.data_ptr(), M, N, K, L, *schedule,
                                        stream=stream)
@@ -78,15 +78,16 @@ def run_gemm(p, M, N, K, L, schedule=None, alpha=1.0, bias=None, b_pad_rows=0):
     return whole[pad:pad + n_out].reshape(L, N, M)
 
 
-def check(M, N, K, L, seed, schedule=None, alpha=1.0, with_bias=False, b_pad_rows=0):
+def check(M, N, K, L, seed, schedule=None, alpha=1.0, with_bias=False, b_pad_rows=0,
+          activation=0):
     p = synthetic.make_gemm_problem(M, N, K, L, seed=seed)
     bias = None
     if with_bias:
         rng = np.random.default_rng(seed)
         bias = (rng.standard_normal((L, N, M)) * 4).astype(np.float16).view(np.uint16)
     ref, vals, tol = oracle.gemm_small_n(p["a"], p["b"], p["sfa"], p["sfb"], M, N, K, L,
-                                         alpha=alpha, bias=bias)
-    got = run_gemm(p, M, N, K, L, schedule, alpha, bias, b_pad_rows)
+                                         alpha=alpha, bias=bias, activation=activation)
+    got = run_gemm(p, M, N, K, L, schedule, alpha, bias, b_pad_rows, activation)
     parity.assert_parity(got, ref, vals, tol, f"gemm M={M} N={N} K={K} L={L} {schedule}")
     return got
 
@@ -135,6 +136,19 @@ def test_gemm_with_one_vector_uses_the_gemv():
 def test_gemm_alpha_bias_and_padded_b():
     check(517, 6, 1344, 3, seed=11, alpha=-0.75, with_bias=True, b_pad_rows=5)
     check(517, 1, 1344, 3, seed=12, alpha=2.0, with_bias=True, b_pad_rows=3)
+
+
+@pytest.mark.parametrize("activation", [nv.ACT_RELU, nv.ACT_SILU, nv.ACT_GELU_TANH,
+                                        nv.ACT_GELU_ERF])
+@pytest.mark.parametrize("N", [1, 5, 16])
+def test_gemm_activation(activation, N):
+    """alpha scales the sums to about unit spread and the bias (4 sigma)
+    shifts them, so outputs fall on both sides of each activation's knee."""
+    M, K, L = 300, 1024, 2
+    got = check(M, N, K, L, seed=N + 10 * activation, alpha=0.0625, with_bias=True,
+                activation=activation)
+    vals = got.view(np.float16).astype(np.float64)
+    assert (vals > 0).any() and ((vals < 0).any() or activation == nv.ACT_RELU)
 
 
 def test_gemm_zero_k_gives_bias_or_zeros():

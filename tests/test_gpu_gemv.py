@@ -349,6 +349,31 @@ def test_gemv_ex_alpha_bias_and_padded_b(layout, M, K, L, alpha):
     parity.assert_parity(got, ref, vals, sumabs, f"ex M={M} K={K} L={L} alpha={alpha} layout={layout}")
 
 
+@pytest.mark.parametrize("activation", [nv.ACT_RELU, nv.ACT_SILU, nv.ACT_GELU_TANH,
+                                        nv.ACT_GELU_ERF])
+@pytest.mark.parametrize("layout", [nv.SF_PLAIN, nv.SF_PERMUTED_128x4])
+@pytest.mark.parametrize("M,K,L", [(128, 256, 1), (700, 2048, 3), (130, 80, 3)])
+def test_gemv_ex_activation(activation, layout, M, K, L):
+    """Each kernel nvfp4_gemv_ex picks (direct, pipelined, blockwise) with an
+    output scale, a bias and each activation, against the oracle."""
+    p = synthetic.make_problem(M, K, L, seed=M + K + activation)
+    rng = np.random.default_rng(activation)
+    bias = (rng.standard_normal((L, M)) * 2).astype(np.float16).view(np.uint16)
+    _, s, _ = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
+    alpha = float(2.0 / max(np.std(s), 1e-3))
+    ref, vals, tol = oracle.gemv_ex(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L, alpha=alpha,
+                                    bias=bias, activation=activation)
+    a, b, sfa, sfb = device_problem(p, M, K, L, layout)
+    c = torch.full((L * M,), SENTINEL, dtype=torch.float16, device=DEV)
+    bias_d = torch.from_numpy(bias.reshape(-1).copy()).to(DEV)
+    got = _ex_call(a, b, sfa, sfb, c, M, K, L, layout, alpha=alpha, bias=bias_d.data_ptr(),
+                   activation=activation)
+    parity.assert_parity(got, ref, vals, tol,
+                         f"act={activation} M={M} K={K} L={L} layout={layout}")
+    v = got.view(np.float16).astype(np.float64)
+    assert (v > 0).any() and ((v < 0).any() or activation == nv.ACT_RELU)
+
+
 def test_gemv_ex_zero_k_gives_the_bias():
     M, L = 37, 2
     bias = (np.arange(L * M, dtype=np.float32) - 20).astype(np.float16)
