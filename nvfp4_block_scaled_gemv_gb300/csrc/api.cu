@@ -193,23 +193,37 @@ cudaError_t tc_resident_clusters(int stages, int64_t N, int ks, int* out) {
   return cudaSuccess;
 }
 
-// Tensor-core schedule (measured on GB300 over the decode-batch shapes): 2
-// stages per CTA, so the most CTAs share an SM and their copy+MMA chains
-// overlap; the smallest cluster size k_split whose L*ceil(M/128) tiles times
-// k_split fill at least 70% of the resident CTA slots, at least 2 once K has
-// 16 or more 256-element stages (shorter per-tile K ranges), at most 4 when
-// more than 8 columns are summed across the cluster, never more than the K
-// stages; and as many clusters as are resident at once (persistent), but no
-// more than the tiles.  slots = CTAs resident at once.
-void tc_rule(int64_t M, int64_t N, int64_t K, int64_t L, int64_t slots, int* stages,
-             int* k_split, int64_t* ctas) {
+// Tensor-core schedule (measured on GB300 over the decode-batch shapes, cold
+// L2).  slots2 / slots4 = CTAs of 2 / 4 stages resident at once.
+//  * When the L*ceil(M/128) tiles fit in one wave of 4-stage CTAs: 4 stages
+//    (two ring slots per MMA chain, so a chain's next copies are in flight
+//    while it issues MMAs) and the largest cluster size k_split whose tiles
+//    times k_split still fit (at most 4 when more than 8 columns are summed
+//    across the cluster, at most 8, each CTA keeping 2 K stages); one CTA per
+//    tile and rank.  (M7168_N8_K2048_L4: 11.2 us against 11.8 with the rule
+//    below; M7168_N16_K16384_L1: 20.6 against 25.5.)
+//  * Otherwise 2 stages, so the most CTAs share an SM and their copy+MMA
+//    chains overlap; the smallest k_split whose tiles times k_split fill at
+//    least 70% of the resident slots, at least 2 once K has 16 or more
+//    256-element stages, at most 4 when more than 8 columns are summed, never
+//    more than the K stages; and as many clusters as are resident at once
+//    (persistent), but no more than the tiles.
+void tc_rule(int64_t M, int64_t N, int64_t K, int64_t L, int64_t slots2, int64_t slots4,
+             int* stages, int* k_split, int64_t* ctas) {
   const int64_t tiles = L * ((M + 127) / 128);
   const int64_t kst = (K + 255) / 256;
   const int ks_max = N > 8 ? 4 : 8;
   int ks = 1;
-  while (ks < ks_max && 2 * ks <= kst && tiles * ks * 10 < slots * 7) ks *= 2;
+  if (tiles <= slots4) {
+    while (ks < ks_max && 4 * ks <= kst && tiles * 2 * ks <= slots4) ks *= 2;
+    *stages = 4;
+    *k_split = ks;
+    *ctas = tiles * ks;
+    return;
+  }
+  while (ks < ks_max && 2 * ks <= kst && tiles * ks * 10 < slots2 * 7) ks *= 2;
   if (ks == 1 && kst >= 16) ks = 2;
-  const int64_t resident = slots / ks > 0 ? slots / ks : 1;
+  const int64_t resident = slots2 / ks > 0 ? slots2 / ks : 1;
   *stages = 2;
   *k_split = ks;
   *ctas = (tiles < resident ? tiles : resident) * ks;
@@ -242,13 +256,16 @@ void blockdot_rule(int64_t M, int64_t K, int64_t L, bool permuted, int num_sms, 
                                 blockdot_slot_rows(M, L, permuted, n), kBlockDotSmemBudget);
 }
 
-// The rule above with the CTAs of the 2-stage kernel resident on this device.
+// The rule above with the CTAs of the 2- and 4-stage kernels resident on this
+// device.
 cudaError_t plan_tc(int64_t M, int64_t N, int64_t K, int64_t L, int* stages, int* k_split,
                     int64_t* ctas) {
   int slots = 0;
-  const cudaError_t err = tc_resident_clusters(2, N, 1, &slots);
+  int slots4 = 0;
+  cudaError_t err = tc_resident_clusters(2, N, 1, &slots);
+  if (err == cudaSuccess) err = tc_resident_clusters(4, N, 1, &slots4);
   if (err != cudaSuccess) return err;
-  tc_rule(M, N, K, L, slots, stages, k_split, ctas);
+  tc_rule(M, N, K, L, slots, slots4, stages, k_split, ctas);
   return cudaSuccess;
 }
 
@@ -427,11 +444,12 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
   }
   if (kernel == kKernelTensor) {
     if (!permuted || kchunks == 0) return false;
-    // host-only estimate: 4 CTAs of the 2-stage kernel resident per SM
-    // (the launch recomputes the schedule from this device's limits)
+    // host-only estimate: 4 CTAs of the 2-stage kernel or 2 of the 4-stage
+    // kernel resident per SM (the launch recomputes the schedule from this
+    // device's limits)
     int stages = 2, ks = 1;
     int64_t ctas = 1;
-    tc_rule(M, 1, K, L, (int64_t)num_sms * 4, &stages, &ks, &ctas);
+    tc_rule(M, 1, K, L, (int64_t)num_sms * 4, (int64_t)num_sms * 2, &stages, &ks, &ctas);
     out->kernel = kKernelTensor;
     out->lanes_per_row = stages;
     out->k_split = ks;
@@ -717,7 +735,7 @@ nvfp4_status_t nvfp4_gemm_small_n_plan(int64_t M, int64_t N, int64_t K, int64_t 
   if (L * ((M + 127) / 128) > 0x7fffffff) return NVFP4_ERR_UNSUPPORTED_SHAPE;  // 128-row tiles
   cudaError_t err = plan_tc(M, N < 1 ? 1 : N, K, L, stages, k_split, ctas);
   if (err == cudaSuccess && resident_ctas != nullptr)
-    err = tc_resident_clusters(2, N < 1 ? 1 : N, 1, resident_ctas);
+    err = tc_resident_clusters(*stages, N < 1 ? 1 : N, 1, resident_ctas);
   if (err != cudaSuccess) return cuda_failure(err);
   return NVFP4_OK;
 }

@@ -40,8 +40,9 @@
 //
 // Scale signs: the MMA reads each scale byte as an unsigned magnitude, so
 // before a stage's MMAs the MMA warp folds every negative sfa or sfb code into
-// the sign bits of the 16 E2M1 elements it scales (fold_scale_signs); codes
-// with the sign bit clear, the benchmark's, only cost that warp a scan.
+// the sign bits of the 16 E2M1 elements it scales (fold_scale_signs); a stage
+// whose codes all have the sign bit clear (the benchmark's) costs that warp
+// one vote over its scale bytes (any_negative_scale).
 //
 // Every wait on an mbarrier gives up after kWaitNs of global time, counts a
 // timeout in a device word the host can read, and the thread then skips its
@@ -143,6 +144,37 @@ __device__ __forceinline__ bool fold_scale_signs(uint8_t* gen, uint32_t a_tile, 
     }
   }
   return flipped;
+}
+
+__device__ __forceinline__ uint32_t lds_or4(uint32_t addr) {
+  uint32_t x, y, z, w;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(x), "=r"(y), "=r"(z), "=r"(w)
+               : "r"(addr));
+  return x | y | z | w;
+}
+
+// Whether any of the stage's nk sfa and nk sfb atoms holds a code with the
+// sign bit set (a warp vote; the benchmark's codes never do).  Every lane
+// issues its loads (16 bytes per atom) before testing any, so the common
+// all-positive stage costs the MMA warp one round of shared-memory latency;
+// fold_scale_signs then runs only for stages that need it.
+__device__ __forceinline__ bool any_negative_scale(uint32_t sfa_atoms, uint32_t sfb_atoms, int nk,
+                                                   int lane) {
+  uint32_t acc = 0;
+  if (nk == 4) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      acc |= lds_or4(sfa_atoms + 512u * kk + 16u * lane);
+      acc |= lds_or4(sfb_atoms + 512u * kk + 16u * lane);
+    }
+  } else {
+    for (int kk = 0; kk < nk; ++kk) {
+      acc |= lds_or4(sfa_atoms + 512u * kk + 16u * lane);
+      acc |= lds_or4(sfb_atoms + 512u * kk + 16u * lane);
+    }
+  }
+  return __any_sync(0xffffffffu, (acc & 0x80808080u) != 0u);
 }
 
 // S: pipeline stages per CTA (2 or 4; fewer stages let more CTAs share an SM,
@@ -302,11 +334,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();  // (orders lane 0's acquire before the other lanes' reads)
         if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0) {
           // signed scales: fold negative codes into the operands' sign bits
-          const bool flipped =
-              fold_scale_signs(gen, a_s + st * kTcABytes, b_s + st * kTcBBytes,
-                               sfa_s + st * kTcSfBytes, sfb_s + st * kTcSfBytes, nk, lane);
-          if (__any_sync(0xffffffffu, flipped))
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for the tensor cores
+          if (any_negative_scale(sfa_s + st * kTcSfBytes, sfb_s + st * kTcSfBytes, nk, lane)) {
+            const bool flipped =
+                fold_scale_signs(gen, a_s + st * kTcABytes, b_s + st * kTcBBytes,
+                                 sfa_s + st * kTcSfBytes, sfb_s + st * kTcSfBytes, nk, lane);
+            if (__any_sync(0xffffffffu, flipped))
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for the tensor cores
+          }
           __syncwarp();
         }
         if (lane == 0 && ok) {

@@ -208,9 +208,11 @@ def test_plan_for_the_benchmark_shapes(lib, shape, layout, kernel, want):
 def test_tensor_kernel_plans(lib):
     """The tensor-core kernel: pre-permuted scales only, selected explicitly
     (nvfp4_gemv never picks it: its MMA reads scale codes as unsigned); its
-    schedule follows the measured rule (2 stages, the smallest cluster filling
-    70% of 4 resident CTAs per SM, at least 2 for 16+ K stages, persistent
-    clusters no more than the tiles)."""
+    schedule follows the measured rule: tiles that fit one wave of 4-stage
+    CTAs (2 per SM) get 4 stages and the largest cluster that still fits, one
+    CTA per tile and rank; larger problems 2 stages, the smallest cluster
+    filling 70% of 4 resident CTAs per SM, at least 2 for 16+ K stages,
+    persistent clusters no more than the tiles."""
     with pytest.raises(nv.Nvfp4Error):
         nv.nvfp4_gemv_plan(4096, 7168, 8, 0, 152, 2, kernel=nv.KERNEL_TENSOR)
     for shape in ((16384, 8192, 16), (16384, 8192, 2), (16384, 8192, 8), (1, 1024, 1 << 31),
@@ -224,9 +226,14 @@ def test_tensor_kernel_plans(lib):
         plan = nv.nvfp4_gemv_plan(M, K, L, 1, sms, 2, kernel=nv.KERNEL_TENSOR)
         tiles, kst = L * -(-M // 128), -(-K // 256)
         ks = plan["k_split"]
-        assert plan["lanes_per_row"] == 2 and ks in (1, 2, 4, 8) and (ks == 1 or ks <= kst)
+        assert ks in (1, 2, 4, 8) and (ks == 1 or ks <= kst)
         assert plan["ctas"] % ks == 0 and plan["ctas"] // ks <= tiles
-        assert plan["ctas"] <= max(ks, 4 * sms)
+        if tiles <= 2 * sms:  # one wave of 4-stage CTAs
+            assert plan["lanes_per_row"] == 4 and plan["ctas"] == tiles * ks
+            assert plan["ctas"] <= 2 * sms and (ks == 1 or 2 * ks <= kst)
+            assert ks == 8 or 2 * tiles * ks > 2 * sms or 4 * ks > kst
+        else:
+            assert plan["lanes_per_row"] == 2 and plan["ctas"] <= max(ks, 4 * sms)
 
 
 def test_block_dot_plans_and_validation(lib):
