@@ -90,8 +90,9 @@ typedef enum {
  * pages' `assumed_align` of 16 and 32), c 2-byte aligned.  (A 16-byte
  * aligned a is never run on the direct kernel, whose 256-bit loads need 32.)
  * Accuracy: on the CUDA-core kernels each 16-element block's dot product is
- * exact and blocks are scaled and summed in FP32 (nvfp4_gemv always runs one
- * of them).
+ * exact and blocks are scaled and summed in FP32; the tensor-core kernel
+ * (which nvfp4_gemv runs for large pre-permuted streams, see nvfp4_gemv_plan)
+ * sums in FP32 in the MMA's own order.
  * c is rounded to nearest even (overflow gives +-Inf; a NaN scale gives NaN)
  * and stays within 1e-3 * sum|terms| + 1 fp16 ulp of the exact result.
  * Results are bitwise reproducible run to run.  The FP32 summation order
@@ -190,9 +191,10 @@ typedef enum {
    * contract, not the CUDA-core kernels' bits.  The MMA reads scale codes as
    * unsigned magnitudes; the kernel folds every negative sfa or sfb code into
    * the sign bits of the 16 elements it scales before the MMA, so signed,
-   * subnormal and NaN codes give the E4M3 result.  Selected explicitly only
-   * (nvfp4_gemv picks the CUDA-core kernels; nvfp4_gemm_small_n uses it for
-   * N >= 2). */
+   * subnormal and NaN codes give the E4M3 result.  nvfp4_gemv runs it for
+   * pre-permuted scales with at least 768 MB of A, K <= 8192 and M >= 1024,
+   * where it was measured faster than the pipelined kernel;
+   * nvfp4_gemm_small_n uses it for N >= 2. */
   NVFP4_KERNEL_TENSOR = 2,
   /* Tensor-core block dots with the scales applied on the CUDA cores: A is
    * streamed by TMA in one box per tile of up to 128 rows (rows handed out to
@@ -319,9 +321,11 @@ int nvfp4_tensor_wait_timeouts(int reset);
  * ctas_per_sm the number of the CUDA-core kernel's CTAs resident per SM (pass
  * 0 to use the compiled-in default of 2).  nvfp4_gemv picks: the blockwise
  * kernel for K % 64 != 0; the direct kernel for K = 0 and for plain scales up
- * to 512 KB of A; the pipelined kernel otherwise.  For the tensor-core kernel the plan assumes 4 resident
- * CTAs per SM (a launch recomputes its grid from the device's limits); for
- * the block-dot kernel, one CTA per SM and up to 227 KB of shared memory.
+ * to 512 KB of A; the tensor-core kernel for pre-permuted scales with at
+ * least 768 MB of A, K <= 8192 and M >= 1024; the pipelined kernel otherwise.
+ * For the tensor-core kernel the plan assumes 4 resident 2-stage CTAs (or 2
+ * 4-stage ones) per SM; for the block-dot kernel, one CTA per SM and up to
+ * 227 KB of shared memory.
  */
 typedef struct {
   int kernel;         /* nvfp4_kernel_t */

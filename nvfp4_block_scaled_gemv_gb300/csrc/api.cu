@@ -425,9 +425,17 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
   // the general schedule: the same rule was slower for some of them.)
   const bool small_plain = !permuted && kchunks > 0 && a_bytes <= (int64_t(2) << 20);
   const bool tiny = kernel == -1 && small_plain && a_bytes <= (int64_t(512) << 10);
-  // (the block-dot and tensor-core kernels are selected explicitly: measured
-  // on GB300, the pipelined kernel is as fast or faster on every workload)
-  if (kernel == -1) kernel = tiny || kchunks == 0 ? kKernelDirect : kKernelAsync;
+  // Large streams with pre-permuted scales: the tensor-core kernel (measured on
+  // GB300, cold L2, against the pipelined kernel: 5-7% faster from ~900 MB of
+  // A when K <= 8192, e.g. M16384_K8192_L16 173.8 against 182.8 us and
+  // M28672_K8192_L8 154.6 against 166.0; level at 537 MB; slower when
+  // K = 16384 and on most shapes below 512 MB).  The block-dot kernel is
+  // explicit only (level with the pipelined kernel at best).
+  const bool tensor_pays = permuted && K <= 8192 && M >= 1024 &&
+                           a_bytes >= (int64_t(768) << 20) &&
+                           L * ((M + 127) / 128) <= 0x7fffffff;
+  if (kernel == -1)
+    kernel = tiny || kchunks == 0 ? kKernelDirect : tensor_pays ? kKernelTensor : kKernelAsync;
   if (kernel == kKernelBlockDot) {
     if (!blockdot_shape_ok(M, K, L, permuted)) return false;
     int stages = 2;

@@ -182,7 +182,9 @@ BENCH_SHAPES = [(128, 256, 1), (7168, 2048, 4), (4096, 7168, 8), (7168, 16384, 1
     (BENCH_SHAPES[1], 1, -1, (1, 4, 4, 304, 64)),
     (BENCH_SHAPES[2], 1, -1, (1, 16, 1, 304, 16)),
     (BENCH_SHAPES[3], 1, -1, (1, 16, 8, 304, 32)),
-    (BENCH_SHAPES[4], 1, -1, (1, 4, 8, 304, 64)),
+    # >= 768 MB of A with pre-permuted scales and K <= 8192: the tensor-core
+    # kernel, 2 stages, clusters of 2, 304 persistent clusters
+    (BENCH_SHAPES[4], 1, -1, (2, 2, 2, 608, 128)),
     (BENCH_SHAPES[4], 1, 1, (1, 4, 8, 304, 64)),
     (BENCH_SHAPES[1], 0, 3, (3, 5, 1, 152, 128)),  # block-dot: one CTA per SM, 5 ring slots
     (BENCH_SHAPES[3], 1, 3, (3, 11, 1, 152, 128)),
@@ -206,19 +208,22 @@ def test_plan_for_the_benchmark_shapes(lib, shape, layout, kernel, want):
 
 
 def test_tensor_kernel_plans(lib):
-    """The tensor-core kernel: pre-permuted scales only, selected explicitly
-    (nvfp4_gemv never picks it: its MMA reads scale codes as unsigned); its
-    schedule follows the measured rule: tiles that fit one wave of 4-stage
+    """The tensor-core kernel: pre-permuted scales only; its schedule follows
+    the measured rule: tiles that fit one wave of 4-stage
     CTAs (2 per SM) get 4 stages and the largest cluster that still fits, one
     CTA per tile and rank; larger problems 2 stages, the smallest cluster
     filling 70% of 4 resident CTAs per SM, at least 2 for 16+ K stages,
     persistent clusters no more than the tiles."""
     with pytest.raises(nv.Nvfp4Error):
         nv.nvfp4_gemv_plan(4096, 7168, 8, 0, 152, 2, kernel=nv.KERNEL_TENSOR)
-    for shape in ((16384, 8192, 16), (16384, 8192, 2), (16384, 8192, 8), (1, 1024, 1 << 31),
-                  (1, 1024, (1 << 31) - 1)):
-        for layout in (0, 1):
-            assert nv.nvfp4_gemv_plan(*shape, layout, 152, 2)["kernel"] == nv.KERNEL_PIPELINED
+    # nvfp4_gemv takes it for pre-permuted scales from 768 MB of A with K <= 8192
+    # and M >= 1024 (measured faster there); plain scales never
+    T, P = nv.KERNEL_TENSOR, nv.KERNEL_PIPELINED
+    for shape, want in (((16384, 8192, 16), T), ((28672, 8192, 8), T), ((16384, 8192, 8), P),
+                        ((16384, 16384, 8), P), ((16384, 8192, 2), P), ((512, 8192, 512), P),
+                        ((1, 1024, 1 << 31), P), ((1, 1024, (1 << 31) - 1), P)):
+        assert nv.nvfp4_gemv_plan(*shape, 1, 152, 2)["kernel"] == want, shape
+        assert nv.nvfp4_gemv_plan(*shape, 0, 152, 2)["kernel"] == P
     rng = np.random.default_rng(1)
     for _ in range(200):
         M, K, L = int(rng.integers(1, 30000)), 64 * int(rng.integers(1, 400)), int(rng.integers(1, 9))

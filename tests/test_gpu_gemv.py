@@ -135,6 +135,9 @@ def test_full_size_workloads_sampled(name, M, K, L):
         parity.assert_parity(got[li, mi], ref, sums, sumabs, f"{name} layout={layout}")
         assert np.isfinite(parity.half_values(got)).all()
         results[layout] = got
+    # the benchmark's scale codes keep every partial sum exact in fp32, so even
+    # different kernels (M16384_K8192_L16 permuted runs on the tensor cores)
+    # give the same bits in both layouts
     assert np.array_equal(results[nv.SF_PLAIN], results[nv.SF_PERMUTED_128x4])
 
 
