@@ -205,20 +205,25 @@ def gpu_id_for_smi(torch, dev_index: int) -> str:
 # helpers
 # ---------------------------------------------------------------------------
 
-# The GEMV kernels' code: everything under csrc/ but the separate scale-repack
-# kernel and the host planner (whose choice is checked through the recorded
-# schedule instead).
-_NOT_KERNEL_CODE = ("repack.cu", "api.cu")
+# The sources each GEMV kernel is compiled from (the host planner's choice is
+# checked through the recorded schedule instead).
+_COMMON_SOURCES = ("internal.h", "ptx.cuh", "epilogue.cuh")
+KERNEL_SOURCES = {
+    "direct": _COMMON_SOURCES + ("gemv_kernel.cuh", "gemv_plain.cu", "gemv_permuted.cu"),
+    "pipelined": _COMMON_SOURCES + ("gemv_kernel.cuh", "gemv_async.cuh", "gemv_async_plain.cu",
+                                    "gemv_async_permuted.cu"),
+    "tensor": _COMMON_SOURCES + ("tc_ptx.cuh", "gemv_tc.cu"),
+    "blockdot": _COMMON_SOURCES + ("tc_ptx.cuh", "gemv_blockdot.cu"),
+    "blockwise": _COMMON_SOURCES + ("gemv_kernel.cuh", "gemv_blockwise.cu"),
+}
 _SCHEDULE_KEYS = ("kernel", "lanes_per_row", "k_split", "ctas")
 
 
-def kernel_source_hash() -> str:
-    """Hash of the GEMV kernels' sources."""
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the sources one GEMV kernel (a KERNEL_NAMES entry) is built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_block_scaled_gemv_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name in _NOT_KERNEL_CODE:
-            continue
+    for name in sorted(KERNEL_SOURCES[kernel]):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -243,7 +248,9 @@ def profiled_traffic(workload: str, layout: str, schedule: dict):
     with open(path) as f:
         d = json.load(f)
     entry = d.get(f"{workload}/{layout}")
-    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+    kernel = KERNEL_NAMES[schedule["kernel"]]
+    if not entry or entry.get("kernel") != kernel or \
+            entry.get("kernel_source_hash") != kernel_source_hash(kernel):
         return None
     captured = entry.get("schedule") or {}
     if any(captured.get(k) != schedule.get(k) for k in _SCHEDULE_KEYS):

@@ -92,3 +92,18 @@ def test_reference_arm_line_on_rank_zero():
                            "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert line["config"]["workload"] == "M16384_K8192_L16"
     assert line["cpu_baseline"]["cores"] == bench_host_cores()
+
+
+def test_kernel_source_sets_cover_every_kernel_file():
+    """Every source under csrc/ but the host planner and the repack belongs to
+    some GEMV kernel's hash (so a changed kernel voids its recorded traffic)."""
+    import os
+
+    import bench
+
+    csrc = os.path.join(bench.ROOT, "nvfp4_block_scaled_gemv_gb300", "csrc")
+    files = set(os.listdir(csrc)) - {"api.cu", "repack.cu"}
+    listed = set().union(*bench.KERNEL_SOURCES.values())
+    assert files == listed
+    assert set(bench.KERNEL_SOURCES) == set(bench.KERNEL_NAMES)
+    assert len({bench.kernel_source_hash(k) for k in bench.KERNEL_NAMES}) == len(bench.KERNEL_NAMES)
