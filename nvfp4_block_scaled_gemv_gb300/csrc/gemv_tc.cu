@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t b_s = a_s + S * kTcABytes;
   const uint32_t sfa_s = b_s + S * kTcBBytes;
   const uint32_t sfb_s = sfa_s + S * kTcSfBytes;
-  const uint32_t red_s = sfb_s + S * kTcSfBytes;  // this CTA's partial sums [2][NC][128]
+  const uint32_t red_s = sfb_s + S * kTcSfBytes;  // this CTA's partial sums [2][128][NC]
   uint8_t* const gen = tc_smem - raw;            // generic pointer = gen + shared address
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int st) { return bar0 + 8u * st; };
@@ -409,17 +409,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (ks > 1 && rank != 0) {
         // wait until rank 0 has read this buffer's previous use, then publish
         tc::mbar_wait<true>(rfree_bar + 8u * buf, (use & 1u) ^ 1u, ok, &g_tc_timeouts);
+        // this row's NC partials side by side: [buf][row][NC]
 #pragma unroll
-        for (int n = 0; n < NC; ++n) red[(buf * NC + n) * 128 + r] = part[n];
+        for (int n = 0; n < NC; ++n) red[(buf * 128 + r) * NC + n] = part[n];
         tc::mbar_arrive_remote(tc::map_rank(rfull_bar + 8u * buf, 0));
         continue;
       }
       if (ks > 1) {
         const bool got = tc::mbar_wait<true>(rfull_bar + 8u * buf, use & 1u, ok, &g_tc_timeouts);
-        for (uint32_t k = 1; k < ks; ++k) {
+        // each rank's NC partials of this row in vector loads, added in rank order
+        if (got) {
+          const uint32_t own = red_s + 4u * (uint32_t)((buf * 128 + r) * NC);
+          for (uint32_t k = 1; k < ks; ++k) {
+            float v[NC];
+            tc::ld_remote_vec<NC>(tc::map_rank(own, k), v);
 #pragma unroll
-          for (int n = 0; n < NC; ++n)
-            if (got) part[n] += tc::ld_remote_f32(tc::map_rank(red_s + 4u * (uint32_t)((buf * NC + n) * 128 + r), k));
+            for (int n = 0; n < NC; ++n) part[n] += v[n];
+          }
         }
         for (uint32_t k = 1; k < ks; ++k) tc::mbar_arrive_remote(tc::map_rank(rfree_bar + 8u * buf, k));
       }

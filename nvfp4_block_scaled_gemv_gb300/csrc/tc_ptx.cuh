@@ -112,10 +112,23 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
-__device__ __forceinline__ float ld_remote_f32(uint32_t cluster_addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
-  return v;
+// NC consecutive floats at a distributed-shared-memory address (16-byte
+// aligned for NC >= 4), loaded with as few vector loads as fit.
+template <int NC>
+__device__ __forceinline__ void ld_remote_vec(uint32_t cluster_addr, float (&v)[NC]) {
+  if constexpr (NC >= 4) {
+#pragma unroll
+    for (int i = 0; i < NC / 4; ++i)
+      asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(v[4 * i]), "=f"(v[4 * i + 1]), "=f"(v[4 * i + 2]), "=f"(v[4 * i + 3])
+                   : "r"(cluster_addr + 16u * i));
+  } else if constexpr (NC == 2) {
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+                 : "=f"(v[0]), "=f"(v[1])
+                 : "r"(cluster_addr));
+  } else {
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v[0]) : "r"(cluster_addr));
+  }
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
