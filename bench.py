@@ -555,6 +555,7 @@ def config_line(torch, nv, dev, stream, peaks, wname, wM, wK, wL, lay_name, step
             "bytes_per_call": wbytes, "us_per_call": round(wus, 3), "gb_per_s": round(gbs, 1),
             "pct_of_hbm_peak": round(100 * gbs / peaks["hbm_gbs"], 2),
             "single_call_l2_flushed_us": round(smed, 3),
+            "single_call_l2_flushed_min_us": round(smin, 3),
             "single_call_pct_of_hbm_peak": round(100 * sgbs / peaks["hbm_gbs"], 2),
             "rotating_sets": sets, "l2": l2_state(wbytes, sets, l2_bytes(torch, dev)),
             "calls": calls, "windows": windows}
