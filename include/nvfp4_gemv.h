@@ -192,9 +192,10 @@ typedef enum {
    * unsigned magnitudes; the kernel folds every negative sfa or sfb code into
    * the sign bits of the 16 elements it scales before the MMA, so signed,
    * subnormal and NaN codes give the E4M3 result.  nvfp4_gemv runs it for
-   * pre-permuted scales with at least 768 MB of A, K <= 8192 and M >= 1024,
-   * where it was measured faster than the pipelined kernel;
-   * nvfp4_gemm_small_n uses it for N >= 2. */
+   * pre-permuted scales with M >= 1024 where it was measured faster than the
+   * pipelined kernel: at least 768 MB of A with K <= 8192, or 128-row tiles
+   * (L * ceil(M/128)) filling 80-100% of one wave of 2 CTAs per SM with
+   * K >= 6144; nvfp4_gemm_small_n uses it for N >= 2. */
   NVFP4_KERNEL_TENSOR = 2,
   /* Tensor-core block dots with the scales applied on the CUDA cores: A is
    * streamed by TMA in one box per tile of up to 128 rows (rows handed out to
@@ -321,8 +322,9 @@ int nvfp4_tensor_wait_timeouts(int reset);
  * ctas_per_sm the number of the CUDA-core kernel's CTAs resident per SM (pass
  * 0 to use the compiled-in default of 2).  nvfp4_gemv picks: the blockwise
  * kernel for K % 64 != 0; the direct kernel for K = 0 and for plain scales up
- * to 512 KB of A; the tensor-core kernel for pre-permuted scales with at
- * least 768 MB of A, K <= 8192 and M >= 1024; the pipelined kernel otherwise.
+ * to 512 KB of A; the tensor-core kernel for pre-permuted scales with
+ * M >= 1024 and either at least 768 MB of A with K <= 8192, or 80-100% of
+ * 2 * num_sms tiles of 128 rows with K >= 6144; the pipelined kernel otherwise.
  * For the tensor-core kernel the plan assumes 4 resident 2-stage CTAs (or 2
  * 4-stage ones) per SM; for the block-dot kernel, one CTA per SM and up to
  * 227 KB of shared memory.

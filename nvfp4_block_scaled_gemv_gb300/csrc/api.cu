@@ -425,15 +425,23 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
   // the general schedule: the same rule was slower for some of them.)
   const bool small_plain = !permuted && kchunks > 0 && a_bytes <= (int64_t(2) << 20);
   const bool tiny = kernel == -1 && small_plain && a_bytes <= (int64_t(512) << 10);
-  // Large streams with pre-permuted scales: the tensor-core kernel (measured on
-  // GB300, cold L2, against the pipelined kernel: 5-7% faster from ~900 MB of
-  // A when K <= 8192, e.g. M16384_K8192_L16 173.8 against 182.8 us and
-  // M28672_K8192_L8 154.6 against 166.0; level at 537 MB; slower when
-  // K = 16384 and on most shapes below 512 MB).  The block-dot kernel is
-  // explicit only (level with the pipelined kernel at best).
-  const bool tensor_pays = permuted && K <= 8192 && M >= 1024 &&
-                           a_bytes >= (int64_t(768) << 20) &&
-                           L * ((M + 127) / 128) <= 0x7fffffff;
+  // Pre-permuted scales on the tensor-core kernel where it was measured faster
+  // than the pipelined kernel (GB300, cold L2):
+  //  * large streams: from ~900 MB of A with K <= 8192, 5-7% (M16384_K8192_L16
+  //    173.8 against 182.8 us, M28672_K8192_L8 154.6 against 166.0); level
+  //    at 537 MB, slower at K = 16384;
+  //  * one wave: tiles (L*ceil(M/128)) filling 80-100% of the resident 4-stage
+  //    CTAs, one CTA per tile, with K >= 6144: faster on 13 of 14 such shapes
+  //    by 0.4-21% (M4096_K7168_L8 24.6 against 25.1 us), 1% slower at
+  //    K = 4096; with 74% filled (224 tiles) 7% slower.
+  // Elsewhere (a K split, a partial wave, short K) the pipelined kernel is
+  // faster.  The block-dot kernel is explicit only (level at best).
+  const int64_t tc_tiles = L * ((M + 127) / 128);
+  const int64_t slots4 = (int64_t)num_sms * 2;  // 4-stage tensor-core CTAs resident
+  const bool tensor_large = K <= 8192 && a_bytes >= (int64_t(768) << 20);
+  const bool tensor_wave = K >= 6144 && tc_tiles <= slots4 && 5 * tc_tiles >= 4 * slots4;
+  const bool tensor_pays = permuted && M >= 1024 && tc_tiles <= 0x7fffffff &&
+                           (tensor_large || tensor_wave);
   if (kernel == -1)
     kernel = tiny || kchunks == 0 ? kKernelDirect : tensor_pays ? kKernelTensor : kKernelAsync;
   if (kernel == kKernelBlockDot) {

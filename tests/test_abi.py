@@ -180,7 +180,8 @@ BENCH_SHAPES = [(128, 256, 1), (7168, 2048, 4), (4096, 7168, 8), (7168, 16384, 1
     (BENCH_SHAPES[4], 0, -1, (1, 32, 1, 304, 8)),
     (BENCH_SHAPES[0], 1, -1, (1, 4, 1, 64, 32)),  # permuted: the general schedule
     (BENCH_SHAPES[1], 1, -1, (1, 4, 4, 304, 64)),
-    (BENCH_SHAPES[2], 1, -1, (1, 16, 1, 304, 16)),
+    # 256 tiles fill 84% of one wave of 4-stage tensor-core CTAs, K >= 6144
+    (BENCH_SHAPES[2], 1, -1, (2, 4, 1, 256, 128)),
     (BENCH_SHAPES[3], 1, -1, (1, 16, 8, 304, 32)),
     # >= 768 MB of A with pre-permuted scales and K <= 8192: the tensor-core
     # kernel, 2 stages, clusters of 2, 304 persistent clusters
@@ -216,12 +217,15 @@ def test_tensor_kernel_plans(lib):
     persistent clusters no more than the tiles."""
     with pytest.raises(nv.Nvfp4Error):
         nv.nvfp4_gemv_plan(4096, 7168, 8, 0, 152, 2, kernel=nv.KERNEL_TENSOR)
-    # nvfp4_gemv takes it for pre-permuted scales from 768 MB of A with K <= 8192
-    # and M >= 1024 (measured faster there); plain scales never
+    # nvfp4_gemv takes it for pre-permuted scales (M >= 1024) from 768 MB of A
+    # with K <= 8192, and when the tiles fill 80-100% of one wave of 4-stage
+    # CTAs (2 per SM) with K >= 6144 (measured faster there); plain scales never
     T, P = nv.KERNEL_TENSOR, nv.KERNEL_PIPELINED
     for shape, want in (((16384, 8192, 16), T), ((28672, 8192, 8), T), ((16384, 8192, 8), P),
-                        ((16384, 16384, 8), P), ((16384, 8192, 2), P), ((512, 8192, 512), P),
-                        ((1, 1024, 1 << 31), P), ((1, 1024, (1 << 31) - 1), P)):
+                        ((16384, 16384, 8), P), ((16384, 8192, 2), T), ((512, 8192, 512), P),
+                        ((4096, 7168, 8), T), ((31232, 8192, 1), T), ((4864, 7680, 8), T),
+                        ((28672, 8192, 1), P), ((4096, 4096, 8), P), ((4096, 16384, 8), T),
+                        ((39040, 8192, 1), P), ((1, 1024, 1 << 31), P), ((1, 1024, (1 << 31) - 1), P)):
         assert nv.nvfp4_gemv_plan(*shape, 1, 152, 2)["kernel"] == want, shape
         assert nv.nvfp4_gemv_plan(*shape, 0, 152, 2)["kernel"] == P
     rng = np.random.default_rng(1)
@@ -311,7 +315,8 @@ def test_permuted_plans_with_plenty_of_rows_use_narrow_rows(lib):
     # scarce rows: the cost model decides
     assert nv.nvfp4_gemv_plan(2048, 4096, 1, nv.SF_PERMUTED_128x4, 152, 2)["lanes_per_row"] != 4
     # uneven K split (28 steps over 8 warps): the cost model decides
-    assert nv.nvfp4_gemv_plan(4096, 7168, 8, nv.SF_PERMUTED_128x4, 152, 2)["lanes_per_row"] != 4
+    plan = nv.nvfp4_gemv_plan(4096, 7168, 8, nv.SF_PERMUTED_128x4, 152, 2, kernel=nv.KERNEL_PIPELINED)
+    assert plan["lanes_per_row"] != 4
 
 
 def test_gemv_ex_option_validation(lib):
