@@ -181,8 +181,12 @@ typedef enum {
   NVFP4_KERNEL_PIPELINED = 1,
   /* The tensor cores' block-scaled MMA (tcgen05 kind::mxf4nvf4, 16-element
    * E4M3 blocks, M = 128 tiles, b padded to N = 16 with zero rows), fed by
-   * TMA; pre-permuted scales only (the 128x4 atom is the MMA's scale
-   * layout).  k_split = CTAs per cluster (1, 2, 4 or 8, at most ceil(K/256))
+   * TMA.  The 128x4 atom of the pre-permuted layout is the MMA's scale
+   * layout; plain scales (K % 256 == 0, a sfb batch stride that is a
+   * multiple of 16 bytes) arrive as 16 bytes per row and 256-element stage,
+   * and the MMA warp writes them out as atoms in shared memory before the
+   * MMAs (the same atoms, so the same bits as pre-permuted scales).
+   * k_split = CTAs per cluster (1, 2, 4 or 8, at most ceil(K/256))
    * splitting each tile's K range, summed in cluster rank order through
    * distributed shared memory; ctas a multiple of k_split (the clusters are
    * persistent over the L*ceil(M/128) tiles); lanes_per_row = pipeline
@@ -191,9 +195,11 @@ typedef enum {
    * contract, not the CUDA-core kernels' bits.  The MMA reads scale codes as
    * unsigned magnitudes; the kernel folds every negative sfa or sfb code into
    * the sign bits of the 16 elements it scales before the MMA, so signed,
-   * subnormal and NaN codes give the E4M3 result.  nvfp4_gemv runs it for
-   * pre-permuted scales with M >= 1024 where it was measured faster than the
-   * pipelined kernel: at least 768 MB of A with K <= 8192, or 128-row tiles
+   * subnormal and NaN codes give the E4M3 result.  nvfp4_gemv runs it with
+   * M >= 1024 where it was measured faster than the pipelined kernel: at
+   * least 512 MB of A with K <= 8192 (either layout; plain scales with
+   * K % 256 == 0 and, through nvfp4_gemv_ex, a sfb batch stride that is a
+   * multiple of 16), or, for pre-permuted scales, 128-row tiles
    * (L * ceil(M/128)) filling 80-100% of one wave of 2 CTAs per SM with
    * K >= 6144; nvfp4_gemm_small_n uses it for N >= 2. */
   NVFP4_KERNEL_TENSOR = 2,
@@ -322,11 +328,12 @@ int nvfp4_tensor_wait_timeouts(int reset);
  * ctas_per_sm the number of the CUDA-core kernel's CTAs resident per SM (pass
  * 0 to use the compiled-in default of 2).  nvfp4_gemv picks: the blockwise
  * kernel for K % 64 != 0; the direct kernel for K = 0 and for plain scales up
- * to 512 KB of A; the tensor-core kernel for pre-permuted scales with
- * M >= 1024 and either at least 768 MB of A with K <= 8192, or 80-100% of
- * 2 * num_sms tiles of 128 rows with K >= 6144; the pipelined kernel otherwise.
+ * to 512 KB of A; the tensor-core kernel with M >= 1024 and either at least
+ * 512 MB of A with K <= 8192 (plain scales: K % 256 == 0), or, for
+ * pre-permuted scales, 80-100% of 2 * num_sms tiles of 128 rows with
+ * K >= 6144; the pipelined kernel otherwise.
  * For the tensor-core kernel the plan assumes 4 resident 2-stage CTAs (or 2
- * 4-stage ones) per SM; for the block-dot kernel, one CTA per SM and up to
+ * 4-stage ones) per SM (nvfp4_gemm_small_n_plan gives the schedule rule); for the block-dot kernel, one CTA per SM and up to
  * 227 KB of shared memory.
  */
 typedef struct {

@@ -158,7 +158,8 @@ nvfp4_status_t run_gemv(const void* a, const void* b, const void* sfa, const voi
   else if (plan.kernel == kKernelBlockDot)
     err = launch_blockdot(p, permuted, L, plan.lanes_per_row, plan.ctas, stream);
   else if (plan.kernel == kKernelTensor)
-    err = launch_gemv_tc(p, 1, L, K / 2, plan.lanes_per_row, plan.k_split, plan.ctas, stream);
+    err = launch_gemv_tc(p, 1, L, K / 2, plan.lanes_per_row, plan.k_split, plan.ctas, stream,
+                         !permuted);
   else if (plan.kernel == kKernelAsync)
     err = permuted ? launch_async_permuted(p, plan, stream) : launch_async_plain(p, plan, stream);
   else
@@ -202,12 +203,20 @@ cudaError_t tc_resident_clusters(int stages, int64_t N, int ks, int* out) {
 //    across the cluster, at most 8, each CTA keeping 2 K stages); one CTA per
 //    tile and rank.  (M7168_N8_K2048_L4: 11.2 us against 11.8 with the rule
 //    below; M7168_N16_K16384_L1: 20.6 against 25.5.)
-//  * Otherwise 2 stages, so the most CTAs share an SM and their copy+MMA
-//    chains overlap; the smallest k_split whose tiles times k_split fill at
-//    least 70% of the resident slots, at least 2 once K has 16 or more
-//    256-element stages, at most 4 when more than 8 columns are summed, never
-//    more than the K stages; and as many clusters as are resident at once
-//    (persistent), but no more than the tiles.
+//  * When they fit in one wave of 2-stage CTAs: 2 stages, so the most CTAs
+//    share an SM and their copy+MMA chains overlap; the smallest k_split
+//    whose tiles times k_split fill at least 70% of the resident slots, at
+//    least 2 once K has 16 or more 256-element stages, at most 4 when more
+//    than 8 columns are summed, never more than the K stages; and as many
+//    clusters as are resident at once (persistent), but no more than the
+//    tiles.
+//  * Larger problems: 4 stages on every resident 4-stage CTA (persistent
+//    clusters), in clusters of 2 once K has 32 or more stages, else 1.
+//    Measured on 9 GEMV shapes of 0.6-1.2 GB (both scale layouts) and 7
+//    small-N GEMMs: the best schedule of (2 or 4 stages) x (cluster 1, 2, 4)
+//    everywhere but M8192_K12288_L8 (2.5% from it), e.g. M16384_K8192_L16
+//    176.6 us against 182.5 with the rule above, M32768_K8192_L4 90.9 against
+//    100.4, M16384_N16_K8192_L8 93.5 against 129.1.
 void tc_rule(int64_t M, int64_t N, int64_t K, int64_t L, int64_t slots2, int64_t slots4,
              int* stages, int* k_split, int64_t* ctas) {
   const int64_t tiles = L * ((M + 127) / 128);
@@ -219,6 +228,14 @@ void tc_rule(int64_t M, int64_t N, int64_t K, int64_t L, int64_t slots2, int64_t
     *stages = 4;
     *k_split = ks;
     *ctas = tiles * ks;
+    return;
+  }
+  if (tiles > slots2) {
+    ks = kst >= 32 ? 2 : 1;
+    const int64_t resident = slots4 / ks > 0 ? slots4 / ks : 1;
+    *stages = 4;
+    *k_split = ks;
+    *ctas = (tiles < resident ? tiles : resident) * ks;
     return;
   }
   while (ks < ks_max && 2 * ks <= kst && tiles * ks * 10 < slots2 * 7) ks *= 2;
@@ -425,23 +442,27 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
   // the general schedule: the same rule was slower for some of them.)
   const bool small_plain = !permuted && kchunks > 0 && a_bytes <= (int64_t(2) << 20);
   const bool tiny = kernel == -1 && small_plain && a_bytes <= (int64_t(512) << 10);
-  // Pre-permuted scales on the tensor-core kernel where it was measured faster
-  // than the pipelined kernel (GB300, cold L2):
-  //  * large streams: from ~900 MB of A with K <= 8192, 5-7% (M16384_K8192_L16
-  //    173.8 against 182.8 us, M28672_K8192_L8 154.6 against 166.0); level
-  //    at 537 MB, slower at K = 16384;
-  //  * one wave: tiles (L*ceil(M/128)) filling 80-100% of the resident 4-stage
-  //    CTAs, one CTA per tile, with K >= 6144: faster on 13 of 14 such shapes
-  //    by 0.4-21% (M4096_K7168_L8 24.6 against 25.1 us), 1% slower at
-  //    K = 4096; with 74% filled (224 tiles) 7% slower.
+  // The tensor-core kernel where it was measured faster than the pipelined
+  // kernel (GB300, cold L2):
+  //  * large streams, either scale layout (plain: K % 256 == 0): from 512 MB
+  //    of A with K <= 8192, by 2.6-9.4% plain and 1-11% pre-permuted on 7
+  //    shapes of 0.6-1.2 GB (M16384_K8192_L16 plain 176.6 against 182.0 us,
+  //    M65536_K1024_L16 88.9 against 98.2); with plain scales slower at
+  //    K >= 12288 and below 500 MB;
+  //  * one wave, pre-permuted scales: tiles (L*ceil(M/128)) filling 80-100% of
+  //    the resident 4-stage CTAs, one CTA per tile, with K >= 6144: faster on
+  //    13 of 14 such shapes by 0.4-21% (M4096_K7168_L8 24.6 against 25.1 us),
+  //    1% slower at K = 4096; with 74% filled (224 tiles) 7% slower.  (Plain
+  //    scales there: 25.2 against 23.3 us.)
   // Elsewhere (a K split, a partial wave, short K) the pipelined kernel is
   // faster.  The block-dot kernel is explicit only (level at best).
   const int64_t tc_tiles = L * ((M + 127) / 128);
   const int64_t slots4 = (int64_t)num_sms * 2;  // 4-stage tensor-core CTAs resident
-  const bool tensor_large = K <= 8192 && a_bytes >= (int64_t(768) << 20);
-  const bool tensor_wave = K >= 6144 && tc_tiles <= slots4 && 5 * tc_tiles >= 4 * slots4;
-  const bool tensor_pays = permuted && M >= 1024 && tc_tiles <= 0x7fffffff &&
-                           (tensor_large || tensor_wave);
+  const bool tensor_large =
+      K <= 8192 && a_bytes >= (int64_t(512) << 20) && (permuted || K % 256 == 0);
+  const bool tensor_wave =
+      permuted && K >= 6144 && tc_tiles <= slots4 && 5 * tc_tiles >= 4 * slots4;
+  const bool tensor_pays = M >= 1024 && tc_tiles <= 0x7fffffff && (tensor_large || tensor_wave);
   if (kernel == -1)
     kernel = tiny || kchunks == 0 ? kKernelDirect : tensor_pays ? kKernelTensor : kKernelAsync;
   if (kernel == kKernelBlockDot) {
@@ -459,7 +480,8 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
     return true;
   }
   if (kernel == kKernelTensor) {
-    if (!permuted || kchunks == 0) return false;
+    // plain scales: 16-byte scale rows per 256-element stage (K % 256 == 0)
+    if (kchunks == 0 || (!permuted && K % 256 != 0)) return false;
     // host-only estimate: 4 CTAs of the 2-stage kernel or 2 of the 4-stage
     // kernel resident per SM (the launch recomputes the schedule from this
     // device's limits)
@@ -582,8 +604,11 @@ nvfp4_status_t nvfp4_gemv_ex(const void* a, const void* b, const void* sfa, cons
   const bool permuted = sf_layout == NVFP4_SF_PERMUTED_128x4;
   if (!plan_gemv(M, K, L, permuted, -1, sms, occ, &plan)) return NVFP4_ERR_INVALID_VALUE;
   // the direct kernel loads a with 256-bit loads: a 16-byte aligned a takes
-  // the pipelined kernel (K = 0 reads nothing)
-  if (plan.kernel == kKernelDirect && K > 0 && !aligned(a, 32) &&
+  // the pipelined kernel (K = 0 reads nothing); the tensor-core kernel reads
+  // plain sfb rows through a tensor map: a batch stride that is not a
+  // multiple of 16 bytes takes the pipelined kernel
+  if (((plan.kernel == kKernelDirect && K > 0 && !aligned(a, 32)) ||
+       (plan.kernel == kKernelTensor && !permuted && opt.sfb_batch_stride % 16 != 0)) &&
       !plan_gemv(M, K, L, permuted, kKernelAsync, sms, occ, &plan))
     return NVFP4_ERR_INVALID_VALUE;
   return run_gemv(a, b, sfa, sfb, c, M, K, L, sf_layout, plan, opt, (cudaStream_t)stream);
@@ -651,10 +676,12 @@ nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa
   const int64_t steps = (K / 64 + lanes_per_row - 1) / lanes_per_row;
   // the pipelined kernel needs a K range and a step for every K-split warp
   if (kernel == kKernelAsync && (K == 0 || k_split > steps)) return NVFP4_ERR_INVALID_VALUE;
-  // the tensor-core kernel: pre-permuted scales, clusters of k_split CTAs that
-  // each take at least one 256-element K stage of every 128-row tile
+  // the tensor-core kernel: clusters of k_split CTAs that each take at least
+  // one 256-element K stage of every 128-row tile; plain scales with
+  // K % 256 == 0 only
   if (kernel == kKernelTensor) {
-    if (sf_layout != NVFP4_SF_PERMUTED_128x4 || K == 0) return NVFP4_ERR_INVALID_VALUE;
+    if (K == 0) return NVFP4_ERR_INVALID_VALUE;
+    if (!permuted && K % 256 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (k_split > (K + 255) / 256 || ctas % k_split != 0) return NVFP4_ERR_INVALID_VALUE;
     if (L * ((M + 127) / 128) > 0x7fffffff) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   }

@@ -1,5 +1,5 @@
 // NVFP4 block-scaled batched GEMV and small-N GEMM on the tensor cores
-// (tcgen05, sm_103a), pre-permuted scales only.
+// (tcgen05, sm_103a): pre-permuted scales, and plain scales for the GEMV.
 //
 // The hardware block-scaled MMA (kind::mxf4nvf4, 16-element blocks with E4M3
 // scales, scale_vec::4X) computes, for a 128-row tile of A and an N = 16 row
@@ -10,7 +10,12 @@
 // D.  The 128x4 scale atom of the pre-permuted layout is byte for byte the
 // source of one 32x128b.warpx4 TMEM copy, so the scales need no repacking:
 // one sfa atom and one sfb atom (512 B each) feed one MMA.  (An MMA's scale
-// address in TMEM is a 4-column-aligned copy destination.)
+// address in TMEM is a 4-column-aligned copy destination.)  Plain scales (the
+// GEMV, K % 256 == 0): a stage's 16 scale bytes of each of the tile's 128
+// rows arrive as one TMA box, and the MMA warp writes them out as the stage's
+// 4 atoms in shared memory before its TMEM copies (the atoms a repack would
+// have made, so the result is the same bits); a TMA box cannot make the atom
+// itself, whose 4-byte runs are narrower than a box's 16-byte minimum row.
 //
 // One CTA (224 threads):
 //   warp 0      one lane issues the copies of each 256-element K stage: A as
@@ -72,9 +77,12 @@ constexpr uint32_t kTcSfBytes = 4 * 512;    // 4 scale atoms (K = 256)
 // TMEM columns a CTA allocates: accumulators [2 chains][2][16], then sfa and
 // sfb [stage][4 atoms][4 columns] each (a power of two, at least 32).
 __host__ __device__ constexpr uint32_t tc_tmem_cols(int stages) { return stages <= 2 ? 128u : 256u; }
-constexpr uint32_t tc_smem_bytes(int stages, int nc) {
+// Plain scales also stage each K stage's sfa box ([128 rows][16 bytes]) and
+// sfb bytes (16 of a 128-byte slot) before they are laid out as atoms.
+constexpr uint32_t kTcPlainStageBytes = kTcSfBytes + 128;
+constexpr uint32_t tc_smem_bytes(int stages, int nc, bool plain = false) {
   return (uint32_t)stages * (kTcABytes + kTcBBytes + 2 * kTcSfBytes) +
-         2u * (uint32_t)nc * 128u * 4u + 1024u;
+         2u * (uint32_t)nc * 128u * 4u + 1024u + (plain ? (uint32_t)stages * kTcPlainStageBytes : 0u);
 }
 static_assert(64 + 32 * 2 <= tc_tmem_cols(2) && 64 + 32 * 4 <= tc_tmem_cols(4), "TMEM columns");
 // The SM's 512 TMEM columns are never oversubscribed, so an allocation never
@@ -92,6 +100,8 @@ constexpr uint32_t kIdesc = tc::mxf4nvf4_idesc(16);
 struct TcParams {
   CUtensorMap tmap_a;  // uint8 {K/2, M, L}, box {128, 128, 1}, 128-byte swizzle
   CUtensorMap tmap_b;  // uint8 {K/2, N, L}, box {128, N, 1}, 128-byte swizzle
+  CUtensorMap tmap_sfa;  // plain sfa (GEMV): uint8 {K/16, M, L}, box {16, 128, 1}
+  CUtensorMap tmap_sfb;  // plain sfb (GEMV): uint8 {K/16, L} (batch stride sfb_stride), box {16, 1}
   const uint8_t* sfa;  // permuted [L][rest_m][rest_k][512]
   const uint8_t* sfb;  // permuted, one 128-row block per batch (rows 0..N-1): [L][rest_k][512]
   uint16_t* c;         // fp16 [L][N][M]
@@ -177,10 +187,41 @@ __device__ __forceinline__ bool any_negative_scale(uint32_t sfa_atoms, uint32_t 
   return __any_sync(0xffffffffu, (acc & 0x80808080u) != 0u);
 }
 
+// Plain scales (GEMV, N = 1): lane i of the MMA warp turns the staged
+// [128 rows][16 bytes] sfa box of a stage into its 4 atoms (atom kk holds,
+// at byte 16*i + 4*g + b, the scale of block 4*kk + b of row 32*g + i: one
+// 16-byte load per g, one 16-byte store per atom) and lanes 0..3 copy the
+// stage's sfb word kk into row 0 of sfb atom kk (the other rows stay zero).
+// Returns whether any of those codes has the sign bit set (a warp vote).
+__device__ __forceinline__ bool plain_scales_to_atoms(uint8_t* gen, uint32_t staged_sfa,
+                                                      uint32_t staged_sfb, uint32_t sfa_atoms,
+                                                      uint32_t sfb_atoms, int lane) {
+  uint32_t w[4][4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const uint4 v = *reinterpret_cast<const uint4*>(gen + staged_sfa + 16u * (32u * g + lane));
+    w[g][0] = v.x;
+    w[g][1] = v.y;
+    w[g][2] = v.z;
+    w[g][3] = v.w;
+  }
+  const uint32_t sbw = lane < 4 ? *reinterpret_cast<const uint32_t*>(gen + staged_sfb + 4u * lane) : 0u;
+  uint32_t any = sbw;
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    *reinterpret_cast<uint4*>(gen + sfa_atoms + 512u * kk + 16u * lane) =
+        make_uint4(w[0][kk], w[1][kk], w[2][kk], w[3][kk]);
+    any |= w[0][kk] | w[1][kk] | w[2][kk] | w[3][kk];
+  }
+  if (lane < 4) *reinterpret_cast<uint32_t*>(gen + sfb_atoms + 512u * lane) = sbw;
+  return __any_sync(0xffffffffu, (any & 0x80808080u) != 0u);
+}
+
 // S: pipeline stages per CTA (2 or 4; fewer stages let more CTAs share an SM,
 // whose independent copy+MMA chains then overlap).  NC: accumulator columns
-// read back (a power of two >= N, the rows of B that hold data).
-template <int S, int NC>
+// read back (a power of two >= N, the rows of B that hold data).  PLAIN: the
+// GEMV with plain scales (N = 1), which the MMA warps lay out as atoms.
+template <int S, int NC, bool PLAIN>
 __global__ void __launch_bounds__(kTcThreads, 1)
     nvfp4_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t tc_smem[];
@@ -194,6 +235,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sfa_s = b_s + S * kTcBBytes;
   const uint32_t sfb_s = sfa_s + S * kTcSfBytes;
   const uint32_t red_s = sfb_s + S * kTcSfBytes;  // this CTA's partial sums [2][128][NC]
+  const uint32_t stg_s = red_s + 2u * NC * 128u * 4u;  // plain: staged sfa [S][2 KB], sfb [S][128]
+  auto staged_sfa = [&](int st) { return stg_s + (uint32_t)st * kTcSfBytes; };
+  auto staged_sfb = [&](int st) { return stg_s + (uint32_t)S * kTcSfBytes + 128u * st; };
   uint8_t* const gen = tc_smem - raw;            // generic pointer = gen + shared address
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int st) { return bar0 + 8u * st; };
@@ -236,6 +280,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   for (uint32_t i = threadIdx.x; i < S * kTcBBytes / 16; i += kTcThreads)
     if ((int)((i % (kTcBBytes / 16)) / 8) >= p.N)
       *reinterpret_cast<uint4*>(gen + b_s + 16 * i) = make_uint4(0, 0, 0, 0);
+  // plain scales: rows 1..127 of every sfb atom stay zero
+  if constexpr (PLAIN)
+    for (uint32_t i = threadIdx.x; i < S * kTcSfBytes / 16; i += kTcThreads)
+      *reinterpret_cast<uint4*>(gen + sfb_s + 16 * i) = make_uint4(0, 0, 0, 0);
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -285,14 +333,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int c = i & 1, st = c * SC + pos[c];
           if (tc::mbar_wait<false>(empty_bar(st), ph[c] ^ 1u, ok, &g_tc_timeouts)) {
             const uint32_t fb = full_bar(st);
-            tc::mbar_expect_tx(fb, kTcABytes + 128u * (uint32_t)p.N + 2u * (uint32_t)nk * 512u);
+            if constexpr (PLAIN) {
+              // the stage's 16 scale bytes of every row, and of b (a whole box
+              // either way; blocks past K arrive as zeros)
+              tc::mbar_expect_tx(fb, kTcABytes + 128u * (uint32_t)p.N + kTcSfBytes + 16u);
+            } else {
+              tc::mbar_expect_tx(fb, kTcABytes + 128u * (uint32_t)p.N + 2u * (uint32_t)nk * 512u);
+            }
             tc::tma_load_3d(a_s + st * kTcABytes, &p.tmap_a, s * 128, mt * 128, l, fb);
             tc::tma_load_3d(b_s + st * kTcBBytes, &p.tmap_b, s * 128, 0, l, fb);
-            tc::bulk_load(sfa_s + st * kTcSfBytes,
-                      p.sfa + (((int64_t)l * p.rest_m + mt) * p.rest_k + 4 * s) * 512,
-                      (uint32_t)nk * 512u, fb);
-            tc::bulk_load(sfb_s + st * kTcSfBytes, p.sfb + (int64_t)l * p.sfb_stride + (int64_t)s * 2048,
-                      (uint32_t)nk * 512u, fb);
+            if constexpr (PLAIN) {
+              tc::tma_load_3d(staged_sfa(st), &p.tmap_sfa, s * 16, mt * 128, l, fb);
+              tc::tma_load_2d(staged_sfb(st), &p.tmap_sfb, s * 16, l, fb);
+            } else {
+              tc::bulk_load(sfa_s + st * kTcSfBytes,
+                        p.sfa + (((int64_t)l * p.rest_m + mt) * p.rest_k + 4 * s) * 512,
+                        (uint32_t)nk * 512u, fb);
+              tc::bulk_load(sfb_s + st * kTcSfBytes, p.sfb + (int64_t)l * p.sfb_stride + (int64_t)s * 2048,
+                        (uint32_t)nk * 512u, fb);
+            }
             ++issued[c];
           }
           if (++pos[c] == SC) {
@@ -333,8 +392,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) tc::mbar_wait<false>(full_bar(st), ph, ok, &g_tc_timeouts);
         __syncwarp();  // (orders lane 0's acquire before the other lanes' reads)
         if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0) {
+          // plain scales: lay the stage's scales out as atoms first (written
+          // through the generic proxy, read by the tensor cores' copies)
+          bool neg;
+          if constexpr (PLAIN) {
+            neg = plain_scales_to_atoms(gen, staged_sfa(st), staged_sfb(st), sfa_s + st * kTcSfBytes,
+                                        sfb_s + st * kTcSfBytes, lane);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          } else {
+            neg = any_negative_scale(sfa_s + st * kTcSfBytes, sfb_s + st * kTcSfBytes, nk, lane);
+          }
           // signed scales: fold negative codes into the operands' sign bits
-          if (any_negative_scale(sfa_s + st * kTcSfBytes, sfb_s + st * kTcSfBytes, nk, lane)) {
+          if (neg) {
             const bool flipped =
                 fold_scale_signs(gen, a_s + st * kTcABytes, b_s + st * kTcBBytes,
                                  sfa_s + st * kTcSfBytes, sfb_s + st * kTcSfBytes, nk, lane);
@@ -471,10 +540,15 @@ namespace {
 
 using TcKernel = void (*)(TcParams);
 
-// The kernel instance for (stages, columns read back); null if none.
-TcKernel tc_kernel_for(int stages, int nc) {
+// The kernel instance for (stages, columns read back, plain scales); null if
+// none (plain scales: the GEMV, one column).
+TcKernel tc_kernel_for(int stages, int nc, bool plain = false) {
+  if (plain) {
+    if (nc != 1) return nullptr;
+    return stages == 2 ? nvfp4_tc_kernel<2, 1, true> : stages == 4 ? nvfp4_tc_kernel<4, 1, true> : nullptr;
+  }
 #define NVFP4_TC(S_, NC_) \
-  if (stages == S_ && nc == NC_) return nvfp4_tc_kernel<S_, NC_>;
+  if (stages == S_ && nc == NC_) return nvfp4_tc_kernel<S_, NC_, false>;
   NVFP4_TC(2, 1) NVFP4_TC(2, 2) NVFP4_TC(2, 4) NVFP4_TC(2, 8) NVFP4_TC(2, 16)
   NVFP4_TC(4, 1) NVFP4_TC(4, 2) NVFP4_TC(4, 4) NVFP4_TC(4, 8) NVFP4_TC(4, 16)
 #undef NVFP4_TC
@@ -485,8 +559,8 @@ int tc_columns(int64_t n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : n <= 8
 
 cudaError_t tc_launch_config(TcKernel kern, int stages, int nc, cudaLaunchConfig_t& cfg,
                              cudaLaunchAttribute (&attr)[2], int ks, int64_t ctas,
-                             cudaStream_t stream) {
-  const uint32_t smem = tc_smem_bytes(stages, nc);
+                             cudaStream_t stream, bool plain = false) {
+  const uint32_t smem = tc_smem_bytes(stages, nc, plain);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   // all of the unified L1/shared storage as shared memory: the kernel reads
@@ -548,10 +622,13 @@ cudaError_t tc_tmem_never_oversubscribed(bool* ok) {
 }  // namespace
 
 cudaError_t launch_gemv_tc(const GemvParams& gp, int64_t N, int64_t L, int64_t b_row_stride,
-                           int stages, int ks, int64_t ctas, cudaStream_t stream) {
+                           int stages, int ks, int64_t ctas, cudaStream_t stream, bool plain) {
   const int nc = tc_columns(N);
-  TcKernel kern = tc_kernel_for(stages, nc);
+  TcKernel kern = tc_kernel_for(stages, nc, plain);
   if (kern == nullptr || N < 1 || N > 16) return cudaErrorInvalidValue;
+  // plain scales: 16-byte rows of sfa and sfb per stage through tensor maps
+  // (row and batch strides multiples of 16 bytes: K % 256 == 0)
+  if (plain && (gp.half_k % 128 != 0 || gp.sfb_stride % 16 != 0)) return cudaErrorInvalidValue;
   bool tmem_ok = false;
   cudaError_t terr = tc_tmem_never_oversubscribed(&tmem_ok);
   if (terr != cudaSuccess) return terr;
@@ -581,6 +658,23 @@ cudaError_t launch_gemv_tc(const GemvParams& gp, int64_t N, int64_t L, int64_t b
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  if (plain && half_k > 0) {
+    const cuuint64_t blocks = (cuuint64_t)gp.blocks;
+    const cuuint64_t sd[3] = {blocks, (cuuint64_t)gp.M, (cuuint64_t)L};
+    const cuuint64_t ss[2] = {blocks, blocks * (cuuint64_t)gp.M};
+    const cuuint32_t sbox[3] = {16, 128, 1};
+    const cuuint64_t fd[2] = {blocks, (cuuint64_t)L};
+    const cuuint64_t fs[1] = {(cuuint64_t)gp.sfb_stride};
+    const cuuint32_t fbox[2] = {16, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&p.tmap_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(gp.sfa), sd, ss,
+               sbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        encode(&p.tmap_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(gp.sfb), fd, fs,
+               fbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   p.sfa = gp.sfa;
   p.sfb = gp.sfb;
   p.c = gp.c;
@@ -596,7 +690,7 @@ cudaError_t launch_gemv_tc(const GemvParams& gp, int64_t N, int64_t L, int64_t b
   p.tiles = (int32_t)(L * gp.rest_m);
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[2];
-  cudaError_t err = tc_launch_config(kern, stages, nc, cfg, attr, ks, ctas, stream);
+  cudaError_t err = tc_launch_config(kern, stages, nc, cfg, attr, ks, ctas, stream, plain);
   if (err != cudaSuccess) return err;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }

@@ -87,12 +87,14 @@ cudaError_t launch_repack(const uint8_t* src, uint8_t* dst, int64_t rows, int64_
 
 constexpr int kTcThreadsPerCta = 224;  // tensor-core kernel: 7 warps
 
-// Tensor-core kernel (gemv_tc.cu, pre-permuted scales): N (1..16) rows of b
-// (row n at b + l*p.b_stride + n*b_row_stride), c [L][N][M]; stages (2 or 4)
-// per CTA; ctas CTAs in clusters of ks, each cluster splitting a 128-row
-// tile's K range ks ways.
+// Tensor-core kernel (gemv_tc.cu): N (1..16) rows of b (row n at
+// b + l*p.b_stride + n*b_row_stride), c [L][N][M]; stages (2 or 4) per CTA;
+// ctas CTAs in clusters of ks, each cluster splitting a 128-row tile's K
+// range ks ways.  Pre-permuted scales, or with plain (N = 1, K % 256 == 0,
+// p.sfb_stride % 16 == 0) the plain layouts.
 cudaError_t launch_gemv_tc(const GemvParams& p, int64_t N, int64_t L, int64_t b_row_stride,
-                           int stages, int ks, int64_t ctas, cudaStream_t stream);
+                           int stages, int ks, int64_t ctas, cudaStream_t stream,
+                           bool plain = false);
 // Clusters of ks tensor-core CTAs that can be resident at once.
 cudaError_t tc_max_active_clusters(int stages, int64_t N, int ks, int* out);
 // Bounded waits of the tensor-core kernel that gave up (read, then optionally

@@ -145,6 +145,16 @@ __device__ __forceinline__ uint32_t cluster_size() {
   return r;
 }
 
+// Tiled TMA load of a 2D box at (x, y) into shared memory, completing on the
+// mbarrier (transaction bytes = the whole box, out-of-bounds fill included).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
 // Tiled TMA load of a 3D box at (x, y, z) into shared memory, completing on
 // the mbarrier (transaction bytes = the whole box, out-of-bounds fill
 // included).

@@ -133,8 +133,12 @@ def test_tensor_kernel_schedule_validation(lib):
     perm = (64, 64, 64, 64, 64, 300, 1024, 2, nv.SF_PERMUTED_128x4)
     plain = perm[:-1] + (nv.SF_PLAIN,)
     T = nv.KERNEL_TENSOR
-    # pre-permuted scales only
-    assert lib.nvfp4_gemv_explicit(*plain, T, 4, 1, 1, None) == nv.ERR_INVALID_VALUE
+    # plain scales need whole 256-element stages of 16-byte scale rows
+    plain320 = plain[:6] + (320,) + plain[7:]
+    assert lib.nvfp4_gemv_explicit(*plain320, T, 4, 1, 1, None) == nv.ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_gemv_explicit(*plain, T, 4, 8, 8, None) == nv.ERR_INVALID_VALUE
+    plain_zero_k = plain[:6] + (0,) + plain[7:]
+    assert lib.nvfp4_gemv_explicit(*plain_zero_k, T, 4, 1, 1, None) == nv.ERR_INVALID_VALUE
     # every CTA of a cluster needs a 256-element K stage: K = 1024 has 4
     assert lib.nvfp4_gemv_explicit(*perm, T, 4, 8, 8, None) == nv.ERR_INVALID_VALUE
     # whole clusters only
@@ -177,15 +181,16 @@ BENCH_SHAPES = [(128, 256, 1), (7168, 2048, 4), (4096, 7168, 8), (7168, 16384, 1
     (BENCH_SHAPES[1], 0, -1, (1, 16, 1, 304, 16)),
     (BENCH_SHAPES[2], 0, -1, (1, 16, 1, 304, 16)),
     (BENCH_SHAPES[3], 0, -1, (1, 32, 4, 304, 16)),
-    (BENCH_SHAPES[4], 0, -1, (1, 32, 1, 304, 8)),
+    # >= 512 MB of A with K <= 8192 (plain scales: K % 256 == 0): the
+    # tensor-core kernel, 4 stages, clusters of 2 (32 K stages), on every
+    # resident 4-stage CTA
+    (BENCH_SHAPES[4], 0, -1, (2, 4, 2, 304, 128)),
     (BENCH_SHAPES[0], 1, -1, (1, 4, 1, 64, 32)),  # permuted: the general schedule
     (BENCH_SHAPES[1], 1, -1, (1, 4, 4, 304, 64)),
     # 256 tiles fill 84% of one wave of 4-stage tensor-core CTAs, K >= 6144
     (BENCH_SHAPES[2], 1, -1, (2, 4, 1, 256, 128)),
     (BENCH_SHAPES[3], 1, -1, (1, 16, 8, 304, 32)),
-    # >= 768 MB of A with pre-permuted scales and K <= 8192: the tensor-core
-    # kernel, 2 stages, clusters of 2, 304 persistent clusters
-    (BENCH_SHAPES[4], 1, -1, (2, 2, 2, 608, 128)),
+    (BENCH_SHAPES[4], 1, -1, (2, 4, 2, 304, 128)),
     (BENCH_SHAPES[4], 1, 1, (1, 4, 8, 304, 64)),
     (BENCH_SHAPES[1], 0, 3, (3, 5, 1, 152, 128)),  # block-dot: one CTA per SM, 5 ring slots
     (BENCH_SHAPES[3], 1, 3, (3, 11, 1, 152, 128)),
@@ -209,25 +214,33 @@ def test_plan_for_the_benchmark_shapes(lib, shape, layout, kernel, want):
 
 
 def test_tensor_kernel_plans(lib):
-    """The tensor-core kernel: pre-permuted scales only; its schedule follows
-    the measured rule: tiles that fit one wave of 4-stage
+    """The tensor-core kernel: plain scales need K % 256 == 0; its schedule
+    follows the measured rule: tiles that fit one wave of 4-stage
     CTAs (2 per SM) get 4 stages and the largest cluster that still fits, one
-    CTA per tile and rank; larger problems 2 stages, the smallest cluster
-    filling 70% of 4 resident CTAs per SM, at least 2 for 16+ K stages,
-    persistent clusters no more than the tiles."""
+    CTA per tile and rank; tiles that fit one wave of 2-stage CTAs (4 per SM)
+    2 stages, the smallest cluster filling 70% of them, at least 2 for 16+ K
+    stages, persistent clusters no more than the tiles; larger problems 4
+    stages on every resident 4-stage CTA, clusters of 2 from 32 K stages."""
     with pytest.raises(nv.Nvfp4Error):
-        nv.nvfp4_gemv_plan(4096, 7168, 8, 0, 152, 2, kernel=nv.KERNEL_TENSOR)
-    # nvfp4_gemv takes it for pre-permuted scales (M >= 1024) from 768 MB of A
-    # with K <= 8192, and when the tiles fill 80-100% of one wave of 4-stage
-    # CTAs (2 per SM) with K >= 6144 (measured faster there); plain scales never
+        nv.nvfp4_gemv_plan(4096, 7232, 8, 0, 152, 2, kernel=nv.KERNEL_TENSOR)
+    assert nv.nvfp4_gemv_plan(4096, 7168, 8, 0, 152, 2, kernel=nv.KERNEL_TENSOR) == \
+        nv.nvfp4_gemv_plan(4096, 7168, 8, 1, 152, 2, kernel=nv.KERNEL_TENSOR)
+    # nvfp4_gemv takes it (M >= 1024) from 512 MB of A with K <= 8192 (plain
+    # scales: K % 256 == 0), and for pre-permuted scales when the tiles fill
+    # 80-100% of one wave of 4-stage CTAs (2 per SM) with K >= 6144 (measured
+    # faster there)
     T, P = nv.KERNEL_TENSOR, nv.KERNEL_PIPELINED
-    for shape, want in (((16384, 8192, 16), T), ((28672, 8192, 8), T), ((16384, 8192, 8), P),
-                        ((16384, 16384, 8), P), ((16384, 8192, 2), T), ((512, 8192, 512), P),
-                        ((4096, 7168, 8), T), ((31232, 8192, 1), T), ((4864, 7680, 8), T),
-                        ((28672, 8192, 1), P), ((4096, 4096, 8), P), ((4096, 16384, 8), T),
-                        ((39040, 8192, 1), P), ((1, 1024, 1 << 31), P), ((1, 1024, (1 << 31) - 1), P)):
-        assert nv.nvfp4_gemv_plan(*shape, 1, 152, 2)["kernel"] == want, shape
-        assert nv.nvfp4_gemv_plan(*shape, 0, 152, 2)["kernel"] == P
+    for shape, perm, plain in (((16384, 8192, 16), T, T), ((28672, 8192, 8), T, T),
+                               ((16384, 8192, 8), T, T), ((16383, 8192, 8), P, P),
+                               ((16384, 16384, 8), P, P), ((16384, 8192, 2), T, P),
+                               ((512, 8192, 512), P, P), ((4096, 7168, 8), T, P),
+                               ((31232, 8192, 1), T, P), ((4864, 7680, 8), T, P),
+                               ((28672, 8192, 1), P, P), ((4096, 4096, 8), P, P),
+                               ((4096, 16384, 8), T, P), ((39040, 8192, 1), P, P),
+                               ((65536, 1024, 16), T, T), ((65536, 1088, 16), T, P),
+                               ((1, 1024, 1 << 31), P, P), ((1, 1024, (1 << 31) - 1), P, P)):
+        assert nv.nvfp4_gemv_plan(*shape, 1, 152, 2)["kernel"] == perm, shape
+        assert nv.nvfp4_gemv_plan(*shape, 0, 152, 2)["kernel"] == plain, shape
     rng = np.random.default_rng(1)
     for _ in range(200):
         M, K, L = int(rng.integers(1, 30000)), 64 * int(rng.integers(1, 400)), int(rng.integers(1, 9))
@@ -241,8 +254,11 @@ def test_tensor_kernel_plans(lib):
             assert plan["lanes_per_row"] == 4 and plan["ctas"] == tiles * ks
             assert plan["ctas"] <= 2 * sms and (ks == 1 or 2 * ks <= kst)
             assert ks == 8 or 2 * tiles * ks > 2 * sms or 4 * ks > kst
-        else:
+        elif tiles <= 4 * sms:  # one wave of 2-stage CTAs
             assert plan["lanes_per_row"] == 2 and plan["ctas"] <= max(ks, 4 * sms)
+        else:  # 4 stages on every resident 4-stage CTA, clusters of 2 from 32 K stages
+            assert plan["lanes_per_row"] == 4 and ks == (2 if kst >= 32 else 1)
+            assert plan["ctas"] == max(1, 2 * sms // ks) * ks
 
 
 def test_block_dot_plans_and_validation(lib):
@@ -366,6 +382,10 @@ def test_plan_invariants_on_random_shapes(lib):
         plan = nv.nvfp4_gemv_plan(M, K, L, 0, sms, 2)
         kch = K // 64
         tiny = M * L * (K // 2) <= 512 << 10
+        tensor = M >= 1024 and 0 < K <= 8192 and K % 256 == 0 and M * L * (K // 2) >= 512 << 20
+        if tensor:  # large plain streams: the tensor-core kernel (checked elsewhere)
+            assert plan["kernel"] == nv.KERNEL_TENSOR
+            continue
         assert plan["kernel"] == (nv.KERNEL_PIPELINED if kch and not tiny else nv.KERNEL_DIRECT)
         if kch and tiny:  # narrow rows, at most 4 K steps split over warps, 8 KB of A per CTA
             assert plan["steps"] <= 4 or plan["lanes_per_row"] == 32

@@ -1,6 +1,7 @@
 """GPU parity of the tensor-core kernel (NVFP4_KERNEL_TENSOR) against the CPU oracle.
 
-The kernel takes pre-permuted scales only.  Every launch is checked for
+Pre-permuted scales, and plain scales when K % 256 == 0 (the kernel lays a
+stage's plain scale rows out as atoms in shared memory).  Every launch is checked for
 writes outside c (sentinel slack) and for bounded pipeline waits that ran out
 (nvfp4_tensor_wait_timeouts must stay 0).  Tolerance as for the CUDA-core
 kernels: |gpu - oracle| <= 1e-3 * sum|terms| + 1 fp16 ulp of the oracle value.
@@ -35,17 +36,23 @@ def to_dev(x):
     return torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
 
 
-def run_tc(a, b, sfa_plain, sfb_plain, M, K, L, ks, ctas, stages=4):
+PERM, PLAIN = nv.SF_PERMUTED_128x4, nv.SF_PLAIN
+
+
+def run_tc(a, b, sfa_plain, sfb_plain, M, K, L, ks, ctas, stages=4, layout=PERM):
     """One tensor-core launch (stages per CTA, clusters of ks) on oracle-repacked
-    scales; returns c's fp16 bits [L, M]."""
-    sfa = to_dev(oracle.repack_scales(sfa_plain, M, K, L))
-    sfb = to_dev(oracle.repack_scales(np.asarray(sfb_plain).reshape(L, 1, K // 16), 1, K, L))
+    scales, or on the plain ones; returns c's fp16 bits [L, M]."""
+    if layout == PERM:
+        sfa = to_dev(oracle.repack_scales(sfa_plain, M, K, L))
+        sfb = to_dev(oracle.repack_scales(np.asarray(sfb_plain).reshape(L, 1, K // 16), 1, K, L))
+    else:
+        sfa, sfb = to_dev(sfa_plain), to_dev(sfb_plain)
     ad, bd = to_dev(a), to_dev(b)
     pad = 64
     buf = torch.full((L * M + 2 * pad,), SENTINEL, dtype=torch.float16, device=DEV)
     c = buf[pad:pad + L * M]
     nv.nvfp4_gemv_explicit(ad.data_ptr(), bd.data_ptr(), sfa.data_ptr(), sfb.data_ptr(),
-                           c.data_ptr(), M, K, L, nv.SF_PERMUTED_128x4, nv.KERNEL_TENSOR, stages, ks,
+                           c.data_ptr(), M, K, L, layout, nv.KERNEL_TENSOR, stages, ks,
                            ctas, torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert nv.nvfp4_tensor_wait_timeouts(reset=True) == 0, "a pipeline wait ran out"
@@ -55,10 +62,11 @@ def run_tc(a, b, sfa_plain, sfb_plain, M, K, L, ks, ctas, stages=4):
     return whole[pad:pad + L * M].reshape(L, M)
 
 
-def check(p, M, K, L, ks, ctas, stages=4):
+def check(p, M, K, L, ks, ctas, stages=4, layout=PERM):
     ref, sums, sumabs = oracle.gemv(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L)
-    got = run_tc(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L, ks, ctas, stages)
-    parity.assert_parity(got, ref, sums, sumabs, f"tensor M={M} K={K} L={L} ks={ks} ctas={ctas}")
+    got = run_tc(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L, ks, ctas, stages, layout)
+    parity.assert_parity(got, ref, sums, sumabs,
+                         f"tensor M={M} K={K} L={L} ks={ks} ctas={ctas} layout={layout}")
     return got
 
 
@@ -98,7 +106,20 @@ TC_CASES = [
 @pytest.mark.parametrize("M,K,L,ks,ctas", TC_CASES)
 def test_parity_tensor_kernel(M, K, L, ks, ctas, stages):
     p = synthetic.make_problem(M, K, L, seed=M + K + ks)
-    check(p, M, K, L, ks, ctas, stages)
+    got = check(p, M, K, L, ks, ctas, stages)
+    if K % 256 == 0:
+        # plain scales: the same MMAs on the same atoms, so the same bits
+        assert np.array_equal(got, check(p, M, K, L, ks, ctas, stages, PLAIN))
+
+
+def test_plain_scales_ragged_rows_and_stage_counts():
+    # plain scale boxes of 128 rows x 16 bytes: rows past M arrive as zeros,
+    # and every K % 256 == 0 gives whole stages (odd stage counts included)
+    for M, K, L in ((1, 256, 3), (7, 768, 2), (129, 1280, 2), (333, 2816, 1)):
+        p = synthetic.make_problem(M, K, L, seed=M * K)
+        check(p, M, K, L, 1, 4, 4, PLAIN)
+        ks = min(2, K // 256)  # every rank of a cluster needs a K stage
+        check(p, M, K, L, ks, 2 * ks, 2, PLAIN)
 
 
 def test_tensor_kernel_is_deterministic():
@@ -119,15 +140,17 @@ def test_tensor_kernel_is_deterministic():
 def test_tensor_kernel_full_size(name, ks, ctas, stages):
     _, M, K, L = next(w for w in synthetic.WORKLOADS if w[0] == name)
     p = synthetic.make_problem(M, K, L, seed=0)
-    check(p, M, K, L, ks, ctas, stages)
+    got = check(p, M, K, L, ks, ctas, stages)
+    assert np.array_equal(got, check(p, M, K, L, ks, ctas, stages, PLAIN))
 
 
 FINITE_E4M3 = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
 
 
+@pytest.mark.parametrize("layout", [PERM, PLAIN])
 @pytest.mark.parametrize("M,K,L,ks,ctas,stages", [(300, 1024, 3, 1, 3, 2), (200, 2304, 2, 2, 4, 4),
                                                   (129, 4096, 1, 4, 8, 2)])
-def test_every_e4m3_scale_code(M, K, L, ks, ctas, stages):
+def test_every_e4m3_scale_code(M, K, L, ks, ctas, stages, layout):
     """sfa and sfb from all 254 finite E4M3 codes (negative, -0, subnormal,
     448) and NaN codes: the MMA reads codes as unsigned magnitudes, and the
     kernel folds negative codes into the operands' sign bits."""
@@ -140,13 +163,14 @@ def test_every_e4m3_scale_code(M, K, L, ks, ctas, stages):
     p["sfa"][L - 1, 77, 60] = 0xFF
     if L > 1:
         p["sfb"][0, 33] = 0xFF  # every output of batch 0 NaN
-    got = check(p, M, K, L, ks, ctas, stages)
+    got = check(p, M, K, L, ks, ctas, stages, layout)
     v = parity.half_values(got)
     assert np.isnan(v[0, 5]) and np.isnan(v[L - 1, 77]) and (L == 1 or np.isnan(v[0]).all())
     assert np.signbit(v[np.isfinite(v)]).any()
 
 
-def test_each_scale_code_alone():
+@pytest.mark.parametrize("layout", [PERM, PLAIN])
+def test_each_scale_code_alone(layout):
     """Row m: a = b = 1.0, sfb = 1.0, sfa code m on block 0 and 0 elsewhere:
     c[m] = 16 * E4M3(m) exactly; then every sfb code across batches."""
     K = 256
@@ -159,7 +183,7 @@ def test_each_scale_code_alone():
     sfa = np.zeros((L, M, K // 16), np.uint8)
     sfa[0, :, 0] = np.arange(256, dtype=np.uint8)
     sfb = np.full((L, K // 16), 0x38, np.uint8)
-    got = parity.half_values(run_tc(a, b, sfa, sfb, M, K, L, 1, 2, 2))[0]
+    got = parity.half_values(run_tc(a, b, sfa, sfb, M, K, L, 1, 2, 2, layout))[0]
     assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], want[~nan])
     M, L = 8, 256
     a = np.full((L, M, K // 2), 0x22, np.uint8)
@@ -168,5 +192,5 @@ def test_each_scale_code_alone():
     sfa[:, :, 0] = 0x38
     sfb = np.zeros((L, K // 16), np.uint8)
     sfb[:, 0] = np.arange(256, dtype=np.uint8)
-    got = parity.half_values(run_tc(a, b, sfa, sfb, M, K, L, 1, 64, 4))[:, 3]
+    got = parity.half_values(run_tc(a, b, sfa, sfb, M, K, L, 1, 64, 4, layout))[:, 3]
     assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], want[~nan])
