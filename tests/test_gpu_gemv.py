@@ -467,14 +467,17 @@ def test_k16_large_sampled():
         parity.assert_parity(got[li, mi], ref, sums, sumabs, f"M={M} K={K} layout={layout}")
 
 
-def test_large_permuted_stream_runs_on_tensor_cores_with_options():
-    """>= 768 MB of A with pre-permuted scales (nvfp4_gemv's tensor-core
-    route): alpha, an fp16 bias, SiLU and b / sfb in padded buffers, sampled
-    outputs against the oracle; the plain call's bits equal the pipelined
-    kernel's (exact sums on the benchmark's scale codes)."""
+@pytest.mark.parametrize("layout", [nv.SF_PLAIN, nv.SF_PERMUTED_128x4])
+def test_large_stream_runs_on_tensor_cores_with_options(layout):
+    """>= 512 MB of A with K <= 8192 (nvfp4_gemv's tensor-core route, plain
+    scales laid out as atoms in shared memory): alpha, an fp16 bias, SiLU and
+    b / sfb in padded buffers, sampled outputs against the oracle; the plain
+    call's bits equal the pipelined kernel's (exact sums on the benchmark's
+    scale codes).  With plain scales, a sfb batch stride that is not a
+    multiple of 16 bytes takes the pipelined kernel, with the same bits."""
     M, K, L = 16384, 8192, 12
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert nv.nvfp4_gemv_plan(M, K, L, nv.SF_PERMUTED_128x4, sms, 0)["kernel"] == nv.KERNEL_TENSOR
+    assert nv.nvfp4_gemv_plan(M, K, L, layout, sms, 0)["kernel"] == nv.KERNEL_TENSOR
     p = synthetic.make_problem(M, K, L, seed=31)
     rng = np.random.default_rng(5)
     mi, li = _sample_indices(M, L, 4000, rng)
@@ -485,20 +488,20 @@ def test_large_permuted_stream_runs_on_tensor_cores_with_options():
     y = oracle.activate(alpha * sums + bias.view(np.float16).astype(np.float64)[li, mi], oracle.ACT_SILU)
     ref_ex = oracle.fp16_rne(y)
     tol_ex = oracle.LIPSCHITZ[oracle.ACT_SILU] * abs(alpha) * sumabs
-    a, b, sfa, sfb = device_problem(p, M, K, L, nv.SF_PERMUTED_128x4, via_gpu_repack=True)
+    a, b, sfa, sfb = device_problem(p, M, K, L, layout, via_gpu_repack=True)
     # plain call: tensor cores, against the oracle and against the pipelined kernel
     c = torch.empty(L * M, dtype=torch.float16, device=DEV)
     stream = torch.cuda.current_stream().cuda_stream
     nv.nvfp4_gemv(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(), c.data_ptr(), M, K, L,
-                  nv.SF_PERMUTED_128x4, stream)
+                  layout, stream)
     torch.cuda.synchronize()
     assert nv.nvfp4_tensor_wait_timeouts(reset=True) == 0
     got = bits(c).reshape(L, M)
     parity.assert_parity(got[li, mi], ref, sums, sumabs, "tensor route, plain call")
-    plan = nv.nvfp4_gemv_plan(M, K, L, nv.SF_PERMUTED_128x4, sms, 0, kernel=nv.KERNEL_PIPELINED)
+    plan = nv.nvfp4_gemv_plan(M, K, L, layout, sms, 0, kernel=nv.KERNEL_PIPELINED)
     c2 = torch.empty_like(c)
     nv.nvfp4_gemv_explicit(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(), c2.data_ptr(),
-                           M, K, L, nv.SF_PERMUTED_128x4, nv.KERNEL_PIPELINED, plan["lanes_per_row"],
+                           M, K, L, layout, nv.KERNEL_PIPELINED, plan["lanes_per_row"],
                            plan["k_split"], plan["ctas"], stream=stream)
     torch.cuda.synchronize()
     assert np.array_equal(bits(c2).reshape(L, M), got)
@@ -511,10 +514,22 @@ def test_large_permuted_stream_runs_on_tensor_cores_with_options():
     bias_d = torch.from_numpy(bias.reshape(-1).copy()).to(DEV)
     c3 = torch.full((L * M,), SENTINEL, dtype=torch.float16, device=DEV)
     nv.nvfp4_gemv_ex(a.data_ptr(), b_pad.data_ptr(), sfa.data_ptr(), sfb_pad.data_ptr(), c3.data_ptr(),
-                     M, K, L, nv.SF_PERMUTED_128x4, alpha=alpha, bias=bias_d.data_ptr(),
+                     M, K, L, layout, alpha=alpha, bias=bias_d.data_ptr(),
                      b_batch_stride=K, sfb_batch_stride=2 * dense, stream=stream,
                      activation=nv.ACT_SILU)
     torch.cuda.synchronize()
     assert nv.nvfp4_tensor_wait_timeouts(reset=True) == 0
     got3 = bits(c3).reshape(L, M)
     parity.assert_parity(got3[li, mi], ref_ex, y, tol_ex, "tensor route with options")
+    if layout == nv.SF_PLAIN:
+        # sfb rows 4 bytes apart from 16-byte alignment: the pipelined kernel
+        odd = dense + 4
+        sfb_odd = torch.full((L, odd), 0x7F, dtype=torch.uint8, device=DEV)
+        sfb_odd[:, :dense] = sfb.view(L, dense)
+        c4 = torch.full((L * M,), SENTINEL, dtype=torch.float16, device=DEV)
+        nv.nvfp4_gemv_ex(a.data_ptr(), b_pad.data_ptr(), sfa.data_ptr(), sfb_odd.data_ptr(),
+                         c4.data_ptr(), M, K, L, layout, alpha=alpha, bias=bias_d.data_ptr(),
+                         b_batch_stride=K, sfb_batch_stride=odd, stream=stream,
+                         activation=nv.ACT_SILU)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(c4).reshape(L, M), got3)

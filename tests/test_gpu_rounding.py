@@ -50,7 +50,7 @@ def _runs(M, K, L, layout):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     out = [("default", None)]
     kernels = [nv.KERNEL_PIPELINED, nv.KERNEL_BLOCKDOT, nv.KERNEL_BLOCKWISE]
-    if layout == nv.SF_PERMUTED_128x4:
+    if layout == nv.SF_PERMUTED_128x4 or K % 256 == 0:
         kernels.append(nv.KERNEL_TENSOR)
     for k in kernels:
         plan = nv.nvfp4_gemv_plan(M, K, L, layout, sms, 0, kernel=k)
@@ -62,6 +62,7 @@ def _runs(M, K, L, layout):
 @pytest.mark.parametrize("name,M,K,L,layout", [
     ("M7168_K16384_L1", 7168, 16384, 1, nv.SF_PLAIN),
     ("M7168_K16384_L1", 7168, 16384, 1, nv.SF_PERMUTED_128x4),
+    ("M16384_K8192_L16", 16384, 8192, 16, nv.SF_PLAIN),
     ("M16384_K8192_L16", 16384, 8192, 16, nv.SF_PERMUTED_128x4),
 ])
 def test_full_size_with_rounding(name, M, K, L, layout):
