@@ -10,8 +10,12 @@
 
 namespace nvfp4 {
 
-// act(y) in fp32 (the codes of nvfp4_activation_t); NaN stays NaN.
-__device__ __forceinline__ float activate(float y, int act) {
+// act(y) in fp32 (the codes of nvfp4_activation_t); NaN stays NaN.  Kept out
+// of line: every kernel's epilogue runs once per output, at the end of a CTA's
+// work, from a cold instruction cache, and the inlined transcendental code of
+// every output column made that tail measurably longer for calls that use no
+// activation.
+static __device__ __noinline__ float activate(float y, int act) {
   switch (act) {
     case 1:  // ReLU (+0 for y <= 0)
       return y > 0.f ? y : (y != y ? y : 0.f);

@@ -113,6 +113,13 @@ struct TcParams {
   int32_t activation;  // nvfp4_activation_t
 };
 
+// A CTA's first K stages whose A lines are prefetched into the L2 before the
+// dependency wait (the copies themselves wait for it).  Measured on GB300 with
+// back-to-back calls: 2 beat 0, 4 and 8 (M7168_N8_K2048_L4 9.17 us against
+// 10.18, 9.47 and 9.78; M4096_K7168_L8 23.6 against 24.2-24.0); each prefetch
+// costs the producer lane about as much as a copy.
+constexpr int kTcPrefetchStages = 2;
+
 
 // The MMA reads each scale byte as an unsigned E4M3 magnitude (the sign bit
 // is ignored).  A negative scale is folded into the operand it scales: for
@@ -125,7 +132,7 @@ struct TcParams {
 // element was flipped (the caller then fences the writes for the tensor
 // cores).  B rows past the tile's 16 are never written (their atom rows are
 // padding).
-__device__ __forceinline__ bool fold_scale_signs(uint8_t* gen, uint32_t a_tile, uint32_t b_tile,
+static __device__ __noinline__ bool fold_scale_signs(uint8_t* gen, uint32_t a_tile, uint32_t b_tile,
                                                  uint32_t sfa_atoms, uint32_t sfb_atoms, int nk,
                                                  int lane) {
   bool flipped = false;
@@ -294,7 +301,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   tc::fence_before();
   __syncthreads();
-  tc::cluster_sync();  // every CTA's barriers are initialised before any remote arrive
+  // every CTA's barriers are initialised before any remote arrive (clusters
+  // of one CTA have no remote traffic: the barrier cost them ~0.5 us per CTA)
+  if (ks > 1) tc::cluster_sync();
   tc::fence_after();
   const uint32_t tmem = tmem_slot;
   bool ok = true;
@@ -315,7 +324,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int s0, cnt;
         stage_range(cid, s0, cnt);
         const int l = cid / p.rest_m, mt = cid % p.rest_m;
-        for (int i = 0; i < cnt && i < 2 * S; ++i)
+        for (int i = 0; i < cnt && i < kTcPrefetchStages; ++i)
           tc::tma_prefetch_3d(&p.tmap_a, (s0 + i) * 128, mt * 128, l);
       }
       pdl_wait();
@@ -512,7 +521,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   tc::fence_before();
   __syncthreads();
-  tc::cluster_sync();  // no peer still reads or signals this CTA's shared memory
+  if (ks > 1) tc::cluster_sync();  // no peer still reads or signals this CTA's shared memory
   if (warp == 1) {
     tc::fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
