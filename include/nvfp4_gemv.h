@@ -91,8 +91,8 @@ typedef enum {
  * aligned a is never run on the direct kernel, whose 256-bit loads need 32.)
  * Accuracy: on the CUDA-core kernels each 16-element block's dot product is
  * exact and blocks are scaled and summed in FP32; the tensor-core kernel
- * (which nvfp4_gemv runs for large pre-permuted streams, see nvfp4_gemv_plan)
- * sums in FP32 in the MMA's own order.
+ * (which nvfp4_gemv runs for large streams in either scale layout, see
+ * nvfp4_gemv_plan) sums in FP32 in the MMA's own order.
  * c is rounded to nearest even (overflow gives +-Inf; a NaN scale gives NaN)
  * and stays within 1e-3 * sum|terms| + 1 fp16 ulp of the exact result.
  * Results are bitwise reproducible run to run.  The FP32 summation order
@@ -254,9 +254,9 @@ nvfp4_status_t nvfp4_gemv_explicit(const void* a, const void* b, const void* sfa
  * [L][N][K/16] (one 128-row atom block per batch, rows 0..N-1:
  * nvfp4_repack_scales with rows = N), batch stride sfb_batch_stride
  * (0 = (K/64)*512); c fp16 [L][N][M]; bias fp16 [L][N][M] or NULL.
- * N = 1 is nvfp4_gemv_ex with permuted scales (the CUDA-core GEMV); N >= 2
- * runs the tensor-core kernel (NVFP4_KERNEL_TENSOR), whose cost does not grow
- * with N.  Shapes: M, L >= 0, 0 <= N <= 16 (N > 16: UNSUPPORTED_SHAPE),
+ * N = 1 is nvfp4_gemv_ex with permuted scales (kernel and schedule chosen as
+ * nvfp4_gemv chooses them); N >= 2 runs the tensor-core kernel
+ * (NVFP4_KERNEL_TENSOR), whose cost does not grow with N.  Shapes: M, L >= 0, 0 <= N <= 16 (N > 16: UNSUPPORTED_SHAPE),
  * K % 64 == 0 (K = 0 gives c = fp16(bias) or zeros).  Alignment: a and b
  * 16 bytes, sfa and sfb 32 bytes; c and bias 2 bytes; batch strides as for
  * nvfp4_gemv_ex.
