@@ -35,9 +35,11 @@
  *
  * Ownership and execution: every pointer is device memory owned by the
  * caller (or memory the device can address, such as mapped pinned host
- * memory).  No call allocates, frees, synchronizes or keeps per-call state;
- * all work is enqueued on `stream` (NULL = the legacy default stream), so
- * calls may be captured into CUDA graphs.  Kernels are launched with
+ * memory).  No call allocates, frees, synchronizes or keeps per-call state
+ * (the two wait diagnostics at the end, nvfp4_tensor_wait_timeouts and
+ * nvfp4_selftest_bounded_wait, synchronize); all work is enqueued on
+ * `stream` (NULL = the legacy default stream), so the compute calls may be
+ * captured into CUDA graphs.  Kernels are launched with
  * programmatic stream serialization: they wait for the preceding work on the
  * stream before reading any input, so stream order is preserved.
  *
@@ -319,6 +321,20 @@ int nvfp4_last_cuda_error(void);
  * then not valid).  Synchronises the device; reset != 0 clears the count
  * after reading it.  Returns the count, or -1 on a CUDA error. */
 int nvfp4_tensor_wait_timeouts(int reset);
+
+/* Device self-test of that bounded wait (the one the tensor-core and block-dot
+ * kernels use on their pipeline barriers), made so that a wait runs out
+ * without hanging anything: one warp initialises two shared-memory barriers
+ * for one arrival each, arrives on the first, then waits on phase 0 of each.
+ * Expected: *completed = 1 (the first wait returned at once), *gave_up = 1 (the
+ * second gave up: nothing arrives on it), *timeouts = 1 (the give-up was
+ * counted) and *waited_ns about 2e9 (the wait limit, measured with the global
+ * timer).  The self-test has its own counter (nvfp4_tensor_wait_timeouts is
+ * not changed) and leaves the context usable.  Synchronises `stream`; takes
+ * about 2 s.  NULL outputs give NVFP4_ERR_INVALID_VALUE, a CUDA failure
+ * NVFP4_ERR_CUDA. */
+nvfp4_status_t nvfp4_selftest_bounded_wait(int* completed, int* gave_up, int* timeouts,
+                                           int64_t* waited_ns, struct CUstream_st* stream);
 
 /*
  * Launch plan of nvfp4_gemv, computed on the host only (no GPU needed), for

@@ -38,6 +38,7 @@ EXPORTS = (
     "nvfp4_last_cuda_error",
     "nvfp4_gemv_plan",
     "nvfp4_tensor_wait_timeouts",
+    "nvfp4_selftest_bounded_wait",
     "nvfp4_gemm_small_n",
     "nvfp4_gemm_small_n_explicit",
     "nvfp4_gemm_small_n_plan",
@@ -116,6 +117,9 @@ def library() -> ctypes.CDLL:
     lib.nvfp4_gemm_small_n_plan.restype = I
     lib.nvfp4_tensor_wait_timeouts.argtypes = [I]
     lib.nvfp4_tensor_wait_timeouts.restype = I
+    lib.nvfp4_selftest_bounded_wait.argtypes = [ctypes.POINTER(I), ctypes.POINTER(I),
+                                                ctypes.POINTER(I), ctypes.POINTER(I64), P]
+    lib.nvfp4_selftest_bounded_wait.restype = I
     _lib = lib
     return lib
 
@@ -200,6 +204,18 @@ def nvfp4_last_cuda_error() -> int:
 def nvfp4_tensor_wait_timeouts(reset: bool = False) -> int:
     """Bounded waits of the tensor-core kernel that ran out (synchronises)."""
     return int(library().nvfp4_tensor_wait_timeouts(1 if reset else 0))
+
+
+def nvfp4_selftest_bounded_wait(stream: int = 0) -> dict:
+    """Run the device self-test of the kernels' bounded barrier wait (about 2 s;
+    synchronises): one wait that completes and one that must give up."""
+    completed, gave_up, timeouts = ctypes.c_int(-1), ctypes.c_int(-1), ctypes.c_int(-1)
+    waited = ctypes.c_int64(-1)
+    _check(library().nvfp4_selftest_bounded_wait(ctypes.byref(completed), ctypes.byref(gave_up),
+                                                 ctypes.byref(timeouts), ctypes.byref(waited),
+                                                 stream), "nvfp4_selftest_bounded_wait")
+    return {"completed": completed.value, "gave_up": gave_up.value, "timeouts": timeouts.value,
+            "waited_ns": waited.value}
 
 
 def nvfp4_gemv_plan(M: int, K: int, L: int, sf_layout: int = SF_PLAIN, num_sms: int = 152,

@@ -21,7 +21,7 @@ OBJ_DIR = os.path.join(HERE, "_build")
 
 SOURCES = ["api.cu", "gemv_plain.cu", "gemv_permuted.cu", "gemv_async_plain.cu",
            "gemv_async_permuted.cu", "repack.cu", "gemv_tc.cu", "gemv_blockdot.cu",
-           "gemv_blockwise.cu"]
+           "gemv_blockwise.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]

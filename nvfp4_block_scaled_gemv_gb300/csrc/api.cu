@@ -6,6 +6,7 @@
 
 #include "internal.h"
 #include "nvfp4_gemv.h"
+#include "selftest.h"
 
 namespace nvfp4 {
 
@@ -806,6 +807,20 @@ int nvfp4_tensor_wait_timeouts(int reset) {
     return -1;
   }
   return v + w;
+}
+
+nvfp4_status_t nvfp4_selftest_bounded_wait(int* completed, int* gave_up, int* timeouts,
+                                           int64_t* waited_ns, struct CUstream_st* stream) {
+  if (completed == nullptr || gave_up == nullptr || timeouts == nullptr || waited_ns == nullptr)
+    return NVFP4_ERR_INVALID_VALUE;
+  WaitSelftest r = {};
+  const cudaError_t err = run_wait_selftest((cudaStream_t)stream, &r);
+  if (err != cudaSuccess) return cuda_failure(err);
+  *completed = r.completed;
+  *gave_up = r.gave_up;
+  *timeouts = r.timeouts;
+  *waited_ns = r.waited_ns;
+  return NVFP4_OK;
 }
 
 nvfp4_status_t nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, int sf_layout, int kernel,

@@ -42,6 +42,17 @@ def test_header_declarations_match_binding_and_exports(lib):
     assert set(declared) <= exported
 
 
+def test_wait_selftest_rejects_null_outputs_before_any_launch(lib):
+    import ctypes
+    i = ctypes.c_int(0)
+    w = ctypes.c_int64(0)
+    r = ctypes.byref
+    assert lib.nvfp4_selftest_bounded_wait(None, r(i), r(i), r(w), None) == nv.ERR_INVALID_VALUE
+    assert lib.nvfp4_selftest_bounded_wait(r(i), None, r(i), r(w), None) == nv.ERR_INVALID_VALUE
+    assert lib.nvfp4_selftest_bounded_wait(r(i), r(i), None, r(w), None) == nv.ERR_INVALID_VALUE
+    assert lib.nvfp4_selftest_bounded_wait(r(i), r(i), r(i), None, None) == nv.ERR_INVALID_VALUE
+
+
 def test_header_compiles_as_c(tmp_path):
     src = tmp_path / "t.c"
     src.write_text('#include "nvfp4_gemv.h"\nint main(void){return (int)NVFP4_OK;}\n')

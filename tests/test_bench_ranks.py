@@ -95,14 +95,15 @@ def test_reference_arm_line_on_rank_zero():
 
 
 def test_kernel_source_sets_cover_every_kernel_file():
-    """Every source under csrc/ but the host planner and the repack belongs to
-    some GEMV kernel's hash (so a changed kernel voids its recorded traffic)."""
+    """Every source under csrc/ but the host planner, the repack and the wait
+    self-test (no GEMV launch runs their code) belongs to some GEMV kernel's
+    hash (so a changed kernel voids its recorded traffic)."""
     import os
 
     import bench
 
     csrc = os.path.join(bench.ROOT, "nvfp4_block_scaled_gemv_gb300", "csrc")
-    files = set(os.listdir(csrc)) - {"api.cu", "repack.cu"}
+    files = set(os.listdir(csrc)) - {"api.cu", "repack.cu", "selftest.cu", "selftest.h"}
     listed = set().union(*bench.KERNEL_SOURCES.values())
     assert files == listed
     assert set(bench.KERNEL_SOURCES) == set(bench.KERNEL_NAMES)

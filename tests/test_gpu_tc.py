@@ -194,3 +194,19 @@ def test_each_scale_code_alone(layout):
     sfb[:, 0] = np.arange(256, dtype=np.uint8)
     got = parity.half_values(run_tc(a, b, sfa, sfb, M, K, L, 1, 64, 4, layout))[:, 3]
     assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], want[~nan])
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    # The pipeline barriers' bounded wait, made to run out on purpose in a
+    # one-warp kernel (a barrier phase that nothing completes): it must give
+    # up after its 2 s limit, count the give-up and return; the next launches
+    # then run normally.
+    r = nv.nvfp4_selftest_bounded_wait(torch.cuda.current_stream().cuda_stream)
+    assert r["completed"] == 1, r
+    assert r["gave_up"] == 1, r
+    assert r["timeouts"] == 1, r
+    assert 1.9e9 <= r["waited_ns"] <= 20e9, r
+    assert nv.nvfp4_tensor_wait_timeouts(reset=False) == 0  # its own counter
+    p = synthetic.make_problem(300, 512, 2, seed=11)
+    check(p, 300, 512, 2, ks=2, ctas=8)
+    check(p, 300, 512, 2, ks=1, ctas=3, layout=PLAIN)
