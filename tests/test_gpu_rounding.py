@@ -11,6 +11,7 @@ Every kernel and layout is compared on sampled outputs (random rows plus the
 first, last and atom-boundary rows of every batch) against the oracle,
 |gpu - oracle| <= 1e-3 * sum|terms| + 1 fp16 ulp; the largest
 |gpu - oracle| / tolerance is printed, and reported in the assertion message.
+A second launch of each must repeat every output bit for bit.
 """
 import numpy as np
 import pytest
@@ -76,7 +77,8 @@ def test_full_size_with_rounding(name, M, K, L, layout):
     c = torch.empty(L * M, dtype=torch.float16, device=DEV)
     stream = torch.cuda.current_stream().cuda_stream
     report = []
-    for label, sched in _runs(M, K, L, layout):
+    def launch(sched):
+        c.fill_(0)
         if sched is None:
             nv.nvfp4_gemv(a.data_ptr(), b.data_ptr(), sfa.data_ptr(), sfb.data_ptr(), c.data_ptr(),
                           M, K, L, layout, stream)
@@ -85,7 +87,14 @@ def test_full_size_with_rounding(name, M, K, L, layout):
                                    c.data_ptr(), M, K, L, layout, *sched, stream=stream)
         torch.cuda.synchronize()
         assert nv.nvfp4_tensor_wait_timeouts(reset=True) == 0, "a pipeline wait ran out"
-        got = c.cpu().view(torch.int16).numpy().view(np.uint16).reshape(L, M)[li, mi]
+        return c.cpu().view(torch.int16).numpy().view(np.uint16).reshape(L, M)
+
+    for label, sched in _runs(M, K, L, layout):
+        whole = launch(sched)
+        # run to run, every output's bits repeat (the summation order is fixed
+        # by the schedule, and here the order decides the rounding)
+        assert np.array_equal(whole, launch(sched)), f"{name} layout={layout} {label}: not reproducible"
+        got = whole[li, mi]
         ok, tol, diff = parity.compare(got, ref, sums, sumabs)
         fin = np.isfinite(diff)
         worst = float(np.max(diff[fin] / tol[fin]))
