@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(kBdThreads, 1)
         const int nks = min(NC, p.rest_k - NC * s);
         if (lane == 0) tc::mbar_wait2(full_bar(slot), ph, dfull_bar(d), dph, ok, &g_bd_timeouts);
         __syncwarp();
-        // one verdict for the warp: the TMEM load below is warp-collective
+        // one decision for the warp: the TMEM load below is warp-collective
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         float dot[16 * CB];
         uint32_t sa[NC], sb[NC];
