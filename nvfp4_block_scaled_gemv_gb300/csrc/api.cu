@@ -203,12 +203,11 @@ cudaError_t tc_resident_clusters(int stages, int64_t N, int ks, int* out) {
 //    times k_split still fit (at most 4 when more than 8 columns are summed
 //    across the cluster, at most 8, each CTA keeping 2 K stages); one CTA per
 //    tile and rank.  (M7168_N8_K2048_L4: 11.2 us against 11.8 with the rule
-//    below; M7168_N16_K16384_L1: 20.6 against 25.5.)  Except when the tiles
-//    fill 80-99% of that wave and K has 24 to 32 stages: clusters of 2 on
-//    every resident 4-stage CTA (persistent), which balances the partial wave
-//    (alternating runs on 12 such GEMVs and GEMMs: 0.4-3.9% faster on 9,
-//    within 0.3% on 3, e.g. M4096_K7168_L8 24.33 against 24.56 us; slower
-//    with 8-16 stages, or with the wave exactly full).
+//    below; M7168_N16_K16384_L1: 20.6 against 25.5.)  Tiles filling 80-99% of
+//    the wave with 24-32 K stages get no split either: one CTA per tile, which
+//    skips the cluster barriers, beat clusters of 2 on every resident CTA
+//    by 2.1-3.9% on 9 of 10 such GEMVs and GEMMs in alternating runs and
+//    tied on the 10th (e.g. M4096_K7168_L8 23.28 against 23.98 us).
 //  * When they fit in one wave of 2-stage CTAs: 2 stages, so the most CTAs
 //    share an SM and their copy+MMA chains overlap; the smallest k_split
 //    whose tiles times k_split fill at least 70% of the resident slots, at
@@ -230,12 +229,6 @@ void tc_rule(int64_t M, int64_t N, int64_t K, int64_t L, int64_t slots2, int64_t
   const int ks_max = N > 8 ? 4 : 8;
   int ks = 1;
   if (tiles <= slots4) {
-    if (tiles < slots4 && 5 * tiles >= 4 * slots4 && kst >= 24 && kst <= 32) {
-      *stages = 4;
-      *k_split = 2;
-      *ctas = slots4 / 2 * 2;
-      return;
-    }
     while (ks < ks_max && 4 * ks <= kst && tiles * 2 * ks <= slots4) ks *= 2;
     *stages = 4;
     *k_split = ks;

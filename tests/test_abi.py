@@ -198,9 +198,9 @@ BENCH_SHAPES = [(128, 256, 1), (7168, 2048, 4), (4096, 7168, 8), (7168, 16384, 1
     (BENCH_SHAPES[4], 0, -1, (2, 4, 2, 304, 128)),
     (BENCH_SHAPES[0], 1, -1, (1, 4, 1, 64, 32)),  # permuted: the general schedule
     (BENCH_SHAPES[1], 1, -1, (1, 4, 4, 304, 64)),
-    # 256 tiles fill 84% of one wave of 4-stage tensor-core CTAs, K >= 6144;
-    # 28 K stages: clusters of 2 on every resident 4-stage CTA
-    (BENCH_SHAPES[2], 1, -1, (2, 4, 2, 304, 128)),
+    # 256 tiles fill 84% of one wave of 4-stage tensor-core CTAs, K >= 6144:
+    # the tensor-core kernel, one 4-stage CTA per tile, no K split
+    (BENCH_SHAPES[2], 1, -1, (2, 4, 1, 256, 128)),
     (BENCH_SHAPES[3], 1, -1, (1, 16, 8, 304, 32)),
     (BENCH_SHAPES[4], 1, -1, (2, 4, 2, 304, 128)),
     (BENCH_SHAPES[4], 1, 1, (1, 4, 8, 304, 64)),
@@ -262,9 +262,7 @@ def test_tensor_kernel_plans(lib):
         ks = plan["k_split"]
         assert ks in (1, 2, 4, 8) and (ks == 1 or ks <= kst)
         assert plan["ctas"] % ks == 0 and plan["ctas"] // ks <= tiles
-        if tiles < 2 * sms and 5 * tiles >= 8 * sms and 24 <= kst <= 32:  # a partial wave
-            assert plan["lanes_per_row"] == 4 and ks == 2 and plan["ctas"] == 2 * sms // 2 * 2
-        elif tiles <= 2 * sms:  # one wave of 4-stage CTAs
+        if tiles <= 2 * sms:  # one wave of 4-stage CTAs
             assert plan["lanes_per_row"] == 4 and plan["ctas"] == tiles * ks
             assert plan["ctas"] <= 2 * sms and (ks == 1 or 2 * ks <= kst)
             assert ks == 8 or 2 * tiles * ks > 2 * sms or 4 * ks > kst
