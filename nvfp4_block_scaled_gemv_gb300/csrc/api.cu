@@ -208,13 +208,15 @@ cudaError_t tc_resident_clusters(int stages, int64_t N, int ks, int* out) {
 //    skips the cluster barriers, beat clusters of 2 on every resident CTA
 //    by 2.1-3.9% on 9 of 10 such GEMVs and GEMMs in alternating runs and
 //    tied on the 10th (e.g. M4096_K7168_L8 23.28 against 23.98 us).
-//  * When they fit in one wave of 2-stage CTAs: 2 stages, so the most CTAs
-//    share an SM and their copy+MMA chains overlap; the smallest k_split
-//    whose tiles times k_split fill at least 70% of the resident slots, at
-//    least 2 once K has 16 or more 256-element stages, at most 4 when more
-//    than 8 columns are summed, never more than the K stages; and as many
-//    clusters as are resident at once (persistent), but no more than the
-//    tiles.
+//  * When they fit in one wave of 2-stage CTAs (but not of 4-stage ones): 4
+//    stages on every resident 4-stage CTA (persistent), with clusters of 2
+//    only when that leaves each rank strictly fewer K stages over the waves
+//    of tiles (waves = tiles over resident clusters, rounded up, times the
+//    rank's K stages), else no split.  Alternating runs on 9 such small-N
+//    GEMMs: the best of (2 or 4 stages) x (cluster 1 or 2) or within 1.3% of
+//    it on every one, and 0.9-19% faster than the earlier 2-stage rule (e.g.
+//    M4096_N2_K16384_L12 74.2 against 92.1 us, M10240_N4_K16384_L6 91.3
+//    against 96.5).
 //  * Larger problems: 4 stages on every resident 4-stage CTA (persistent
 //    clusters), in clusters of 2 once K has 32 or more stages, else 1.
 //    Measured on 9 GEMV shapes of 0.6-1.2 GB (both scale layouts) and 7
@@ -243,10 +245,14 @@ void tc_rule(int64_t M, int64_t N, int64_t K, int64_t L, int64_t slots2, int64_t
     *ctas = (tiles < resident ? tiles : resident) * ks;
     return;
   }
-  while (ks < ks_max && 2 * ks <= kst && tiles * ks * 10 < slots2 * 7) ks *= 2;
-  if (ks == 1 && kst >= 16) ks = 2;
-  const int64_t resident = slots2 / ks > 0 ? slots2 / ks : 1;
-  *stages = 2;
+  const int64_t pairs = slots4 / 2;  // resident clusters of 2 four-stage CTAs
+  if (pairs > 0 && kst >= 2) {
+    const int64_t w1 = (tiles + slots4 - 1) / slots4 * kst;
+    const int64_t w2 = (tiles + pairs - 1) / pairs * ((kst + 1) / 2);
+    if (w2 < w1) ks = 2;
+  }
+  const int64_t resident = slots4 / ks > 0 ? slots4 / ks : 1;
+  *stages = 4;
   *k_split = ks;
   *ctas = (tiles < resident ? tiles : resident) * ks;
 }

@@ -230,8 +230,8 @@ def test_tensor_kernel_plans(lib):
     follows the measured rule: tiles that fit one wave of 4-stage
     CTAs (2 per SM) get 4 stages and the largest cluster that still fits, one
     CTA per tile and rank; tiles that fit one wave of 2-stage CTAs (4 per SM)
-    2 stages, the smallest cluster filling 70% of them, at least 2 for 16+ K
-    stages, persistent clusters no more than the tiles; larger problems 4
+    4 stages on every resident 4-stage CTA, clusters of 2 only when that
+    leaves each rank fewer K stages over the waves of tiles; larger problems 4
     stages on every resident 4-stage CTA, clusters of 2 from 32 K stages."""
     with pytest.raises(nv.Nvfp4Error):
         nv.nvfp4_gemv_plan(4096, 7232, 8, 0, 152, 2, kernel=nv.KERNEL_TENSOR)
@@ -266,8 +266,12 @@ def test_tensor_kernel_plans(lib):
             assert plan["lanes_per_row"] == 4 and plan["ctas"] == tiles * ks
             assert plan["ctas"] <= 2 * sms and (ks == 1 or 2 * ks <= kst)
             assert ks == 8 or 2 * tiles * ks > 2 * sms or 4 * ks > kst
-        elif tiles <= 4 * sms:  # one wave of 2-stage CTAs
-            assert plan["lanes_per_row"] == 2 and plan["ctas"] <= max(ks, 4 * sms)
+        elif tiles <= 4 * sms:  # one wave of 2-stage CTAs, not of 4-stage ones
+            slots4, pairs = 2 * sms, sms
+            w1 = -(-tiles // slots4) * kst
+            w2 = -(-tiles // pairs) * -(-kst // 2)
+            assert plan["lanes_per_row"] == 4 and ks == (2 if kst >= 2 and w2 < w1 else 1)
+            assert plan["ctas"] == min(tiles, slots4 // ks) * ks
         else:  # 4 stages on every resident 4-stage CTA, clusters of 2 from 32 K stages
             assert plan["lanes_per_row"] == 4 and ks == (2 if kst >= 32 else 1)
             assert plan["ctas"] == max(1, 2 * sms // ks) * ks
