@@ -203,7 +203,8 @@ typedef enum {
    * K % 256 == 0 and, through nvfp4_gemv_ex, a sfb batch stride that is a
    * multiple of 16), or, for pre-permuted scales, 128-row tiles
    * (L * ceil(M/128)) filling 80-100% of one wave of 2 CTAs per SM with
-   * K >= 6144; nvfp4_gemm_small_n uses it for N >= 2. */
+   * K >= 6144, or more tiles than that wave holds and at least 128 MB of A
+   * (any K); nvfp4_gemm_small_n uses it for N >= 2. */
   NVFP4_KERNEL_TENSOR = 2,
   /* Tensor-core block dots with the scales applied on the CUDA cores: A is
    * streamed by TMA in one box per tile of up to 128 rows (rows handed out to
@@ -347,7 +348,8 @@ nvfp4_status_t nvfp4_selftest_bounded_wait(int* completed, int* gave_up, int* ti
  * to 512 KB of A; the tensor-core kernel with M >= 1024 and either at least
  * 512 MB of A with K <= 8192 (plain scales: K % 256 == 0), or, for
  * pre-permuted scales, 80-100% of 2 * num_sms tiles of 128 rows with
- * K >= 6144; the pipelined kernel otherwise.
+ * K >= 6144 or more than 2 * num_sms such tiles with at least 128 MB of A;
+ * the pipelined kernel otherwise.
  * For the tensor-core kernel the plan assumes 4 resident 2-stage CTAs (or 2
  * 4-stage ones) per SM (nvfp4_gemm_small_n_plan gives the schedule rule); for the block-dot kernel, one CTA per SM and up to
  * 227 KB of shared memory.

@@ -465,6 +465,14 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
   //    13 of 14 such shapes by 0.4-21% (M4096_K7168_L8 24.6 against 25.1 us),
   //    1% slower at K = 4096; with 74% filled (224 tiles) 7% slower.  (Plain
   //    scales there: 25.2 against 23.3 us.)
+  //  * more than one wave of tiles with pre-permuted scales, from 128 MB of
+  //    A, any K: faster on 15 of 16 such shapes of 128 MB-1 GB with K from
+  //    1024 to 16384, by 0.8-8.8% (M32768_K2048_L8 46.5 against 51.0 us,
+  //    M8192_K6144_L8 37.7 against 40.3, M16384_K16384_L8 179.9 against
+  //    185.3), 0.4% slower on M8192_K4096_L8.  Below 128 MB it depends on the
+  //    shape (4 of 10 faster, 6 up to 8% slower); with plain scales, whose
+  //    atom layout costs the MMA warp a step per stage, 5 of 6 such shapes
+  //    were slower.
   // Elsewhere (a K split, a partial wave, short K) the pipelined kernel is
   // faster.  The block-dot kernel is explicit only (level at best).
   const int64_t tc_tiles = L * ((M + 127) / 128);
@@ -473,7 +481,10 @@ bool plan_gemv(int64_t M, int64_t K, int64_t L, bool permuted, int kernel, int n
       K <= 8192 && a_bytes >= (int64_t(512) << 20) && (permuted || K % 256 == 0);
   const bool tensor_wave =
       permuted && K >= 6144 && tc_tiles <= slots4 && 5 * tc_tiles >= 4 * slots4;
-  const bool tensor_pays = M >= 1024 && tc_tiles <= 0x7fffffff && (tensor_large || tensor_wave);
+  const bool tensor_waves =
+      permuted && tc_tiles > slots4 && a_bytes >= (int64_t(128) << 20);
+  const bool tensor_pays =
+      M >= 1024 && tc_tiles <= 0x7fffffff && (tensor_large || tensor_wave || tensor_waves);
   if (kernel == -1)
     kernel = tiny || kchunks == 0 ? kKernelDirect : tensor_pays ? kKernelTensor : kKernelAsync;
   if (kernel == kKernelBlockDot) {

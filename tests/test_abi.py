@@ -239,16 +239,18 @@ def test_tensor_kernel_plans(lib):
         nv.nvfp4_gemv_plan(4096, 7168, 8, 1, 152, 2, kernel=nv.KERNEL_TENSOR)
     # nvfp4_gemv takes it (M >= 1024) from 512 MB of A with K <= 8192 (plain
     # scales: K % 256 == 0), and for pre-permuted scales when the tiles fill
-    # 80-100% of one wave of 4-stage CTAs (2 per SM) with K >= 6144 (measured
-    # faster there)
+    # 80-100% of one wave of 4-stage CTAs (2 per SM) with K >= 6144, or more
+    # than one wave from 128 MB of A with any K (measured faster there)
     T, P = nv.KERNEL_TENSOR, nv.KERNEL_PIPELINED
     for shape, perm, plain in (((16384, 8192, 16), T, T), ((28672, 8192, 8), T, T),
-                               ((16384, 8192, 8), T, T), ((16383, 8192, 8), P, P),
-                               ((16384, 16384, 8), P, P), ((16384, 8192, 2), T, P),
+                               ((16384, 8192, 8), T, T), ((16383, 8192, 8), T, P),
+                               ((16384, 16384, 8), T, P), ((16384, 8192, 2), T, P),
                                ((512, 8192, 512), P, P), ((4096, 7168, 8), T, P),
                                ((31232, 8192, 1), T, P), ((4864, 7680, 8), T, P),
                                ((28672, 8192, 1), P, P), ((4096, 4096, 8), P, P),
-                               ((4096, 16384, 8), T, P), ((39040, 8192, 1), P, P),
+                               ((4096, 16384, 8), T, P), ((39040, 8192, 1), T, P),
+                               ((7168, 65536, 1), P, P), ((32768, 1024, 6), P, P),
+                               ((16384, 1024, 16), T, P), ((16384, 1024, 15), P, P),
                                ((65536, 1024, 16), T, T), ((65536, 1088, 16), T, P),
                                ((1, 1024, 1 << 31), P, P), ((1, 1024, (1 << 31) - 1), P, P)):
         assert nv.nvfp4_gemv_plan(*shape, 1, 152, 2)["kernel"] == perm, shape

@@ -141,6 +141,21 @@ def test_full_size_workloads_sampled(name, M, K, L):
     assert np.array_equal(results[nv.SF_PLAIN], results[nv.SF_PERMUTED_128x4])
 
 
+def test_default_route_takes_the_tensor_cores_for_multi_wave_permuted_streams():
+    # pre-permuted scales, more than one wave of 128-row tiles, 128 MB of A:
+    # nvfp4_gemv picks the tensor-core kernel; scales over 0x01..0x50 so that
+    # the fp32 sums round
+    M, K, L = 16384, 2048, 8
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert nv.nvfp4_gemv_plan(M, K, L, nv.SF_PERMUTED_128x4, sms, 0)["kernel"] == nv.KERNEL_TENSOR
+    p = synthetic.make_problem(M, K, L, seed=12, scale_codes=(0x01, 0x50))
+    mi, li = _sample_indices(M, L, 3000, np.random.default_rng(6))
+    ref, sums, sumabs = oracle.gemv_at(p["a"], p["b"], p["sfa"], p["sfb"], M, K, L, mi, li)
+    got = run(p, M, K, L, nv.SF_PERMUTED_128x4, via_gpu_repack=True)
+    assert nv.nvfp4_tensor_wait_timeouts(reset=True) == 0
+    parity.assert_parity(got[li, mi], ref, sums, sumabs, "M16384_K2048_L8 permuted, default route")
+
+
 def test_hand_worked_golden_values(golden_dir):
     with open(os.path.join(golden_dir, "hand_dots.json")) as f:
         cases = json.load(f)["cases"]
